@@ -1,0 +1,179 @@
+/*
+ * paged_gqa.h -- C ABI of libpaged_gqa.so: attention over a paged KV cache
+ * with grouped-query heads, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (crucible paged attention results: the reference kernel,
+ * the K/V pool layout and the GQA mapping paragraphs; crucible README,
+ * "Layout, and why it was nearly free" and "Prefill scheduling"):
+ *
+ *   for each sequence s, query row r in [0, T_s), q head h:
+ *     g     = h / (num_q_heads / num_kv_heads)           (GQA mapping)
+ *     start = L_s - T_s ; end = start + r                (causal bound)
+ *     for keys j in [0, end]:
+ *       page  = block_tables[s][j / page_size]; slot = j % page_size
+ *       k_j   = k_cache[page][slot][g][:], v_j likewise  (through strides)
+ *       sigma_j = scale * dot(q[s,r,h,:], k_j)
+ *     out[s,r,h,:] = sum_j exp(sigma_j - max sigma) v_j / sum_j exp(sigma_j - max sigma)
+ *
+ * L_s = context_lens[s] counts the cached history plus this call's T_s rows
+ * (their K/V must already be in the pages).  Decode is T_s = 1.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: every pointer argument is device memory owned by the caller
+ *    (except `const pa_params*`, which is host memory read during the call).
+ *    The library allocates nothing and keeps no per-call state; the only
+ *    global memory it uses besides the arguments is the caller's workspace.
+ *  - Asynchrony: calls enqueue work on `stream` and return.  PA_OK means the
+ *    arguments passed host validation and the kernels were launched.
+ *    Host-detectable errors return before anything is launched.
+ *  - Device-detected metadata errors (a block-table entry outside
+ *    [0, num_pages), a context length outside [T_s, max_blocks_per_seq *
+ *    page_size]) never form an out-of-range address: the affected keys are
+ *    skipped, rows with no valid key are written as zeros, and the bits
+ *    below are OR-ed into *dev_status when it is non-NULL.  The caller zeroes
+ *    dev_status before the call if it wants a fresh reading.
+ *  - Graph capture: grid sizes depend only on host-side pa_params fields,
+ *    never on device-resident lengths, so calls can be captured in a CUDA
+ *    graph and replayed with new lengths and tables.
+ *  - Determinism: no value path uses atomics, so a given device returns
+ *    bit-identical results for identical inputs on every run.  With
+ *    deterministic = 1 the split-KV partition is also independent of the
+ *    device (a function of pa_params alone).
+ *  - Supported: head_dim in {64, 128}; page_size in {16, 32};
+ *    num_q_heads % num_kv_heads == 0 with a ratio of at most 16;
+ *    q_dtype == kv_dtype in {PA_F32, PA_F16, PA_BF16}; out_dtype = PA_F32;
+ *    q, k_cache, v_cache and out 16-byte aligned; head_dim contiguous and
+ *    the three cache strides multiples of 16 bytes.
+ */
+#ifndef PAGED_GQA_H
+#define PAGED_GQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_NULL = 1,        /* a required pointer is NULL                  */
+    PA_ERR_SHAPE = 2,       /* inconsistent sizes                           */
+    PA_ERR_DTYPE = 3,       /* unknown dtype code                           */
+    PA_ERR_ALIGN = 4,       /* pointer or stride not 16-byte aligned        */
+    PA_ERR_WORKSPACE = 5,   /* workspace smaller than the *_workspace_size  */
+    PA_ERR_UNSUPPORTED = 6, /* valid but not implemented (head_dim, ...)    */
+    PA_ERR_CUDA = 7         /* a CUDA runtime call failed                   */
+} pa_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define PA_DEV_BAD_PAGE 1u /* a block-table entry outside [0, num_pages) */
+#define PA_DEV_BAD_LEN 2u  /* context_len < T_s or > max_blocks_per_seq * page_size */
+#define PA_DEV_TIMEOUT 4u  /* a bounded device wait gave up */
+
+typedef struct {
+    int32_t num_seqs;           /* B                                           */
+    int32_t num_q_heads;        /* Hq                                          */
+    int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 16           */
+    int32_t head_dim;           /* D: 64 or 128                                */
+    int32_t page_size;          /* P: 16 or 32 tokens per page                 */
+    int32_t num_pages;          /* pages in the pool (valid table entries)     */
+    int32_t max_blocks_per_seq; /* row stride of block_tables                  */
+    int32_t max_context_len;    /* host upper bound on every context_lens[s];
+                                   sizes the split plan and the workspace       */
+    int64_t page_stride;        /* elements between pages; 0 = P*Hkv*D          */
+    int64_t token_stride;       /* elements between slots; 0 = Hkv*D            */
+    int64_t head_stride;        /* elements between kv heads; 0 = D             */
+    float scale;                /* applied to q.k (typically 1/sqrt(D))        */
+    pa_dtype q_dtype;           /* dtype of q                                  */
+    pa_dtype kv_dtype;          /* dtype of k_cache / v_cache (== q_dtype)      */
+    pa_dtype out_dtype;         /* PA_F32                                      */
+    int32_t deterministic;      /* 1: split plan from pa_params alone           */
+    int32_t num_splits;         /* decode: 0 = automatic, else requested count  */
+} pa_params;
+
+/* Fills *p with defaults: contiguous strides, PA_F32 out, automatic splits,
+ * deterministic = 1; sizes and dtypes zero.  Returns p. */
+pa_params *pa_params_init(pa_params *p);
+
+/* Human-readable name of a status code (static storage). */
+const char *pa_status_string(pa_status s);
+
+/* ------------------------------------------------------------------ decode
+ * One query row per sequence: q and out are [B][Hq][D] (row-major), q in
+ * q_dtype, out in f32.  block_tables is [B][max_blocks_per_seq] int32,
+ * context_lens is [B] int32, both on the device.
+ *
+ * Split-KV (crucible README "Split-position attention"; minfer doc 71,
+ * Excerpts F and G): the keys of each (sequence, kv head) are cut into
+ * splits of `split_tokens` keys (a multiple of page_size).  The plan is
+ * fixed by pa_params (never by device lengths), so the grid is constant.
+ */
+
+/* Split plan: *num_splits = S (splits per sequence at max_context_len) and
+ * *split_tokens = keys per split.  Either output may be NULL. */
+pa_status pa_decode_plan(const pa_params *p, int32_t *num_splits, int32_t *split_tokens);
+
+/* Bytes of workspace pa_decode needs (0 when the plan has a single split).
+ * Returns 0 for invalid parameters. */
+size_t pa_decode_workspace_size(const pa_params *p);
+
+/* Decode attention: the split partials (when S > 1) and their combine.
+ * workspace: device memory of at least pa_decode_workspace_size(p) bytes,
+ * 256-byte aligned, contents ignored.  dev_status may be NULL. */
+pa_status pa_decode(const pa_params *p, const void *q, const void *k_cache,
+                    const void *v_cache, const int32_t *block_tables,
+                    const int32_t *context_lens, float *out, void *workspace,
+                    size_t workspace_bytes, uint32_t *dev_status, pa_stream_t stream);
+
+/* The partial step on its own.  For each sequence b, q head h and split i
+ * in [0, num_splits) (num_splits from pa_decode_plan) it writes, with
+ * idx = (b*Hq + h)*num_splits + i:
+ *   partial_ml[2*idx]     = m: the largest scaled score of the split times
+ *                           log2(e) (base-2 units), -inf for an empty split
+ *   partial_ml[2*idx + 1] = l: sum over the split of 2^(score*log2e - m)
+ *   partial_acc[idx*D ..] = sum over the split of 2^(score*log2e - m) v_j
+ *                           (not written for an empty split)
+ * partial_ml is [B][Hq][S][2] f32, partial_acc is [B][Hq][S][D] f32. */
+pa_status pa_decode_partial(const pa_params *p, const void *q, const void *k_cache,
+                            const void *v_cache, const int32_t *block_tables,
+                            const int32_t *context_lens, float *partial_ml,
+                            float *partial_acc, int32_t num_splits,
+                            uint32_t *dev_status, pa_stream_t stream);
+
+/* Combine (crucible README "Split-position attention": rescale each split
+ * by exp(m_i - m_max) and merge; minfer doc 71 Excerpt F: empty splits get
+ * weight zero).  For each (b, h), in ascending split order:
+ *   M = max_i m_i;  w_i = 2^(m_i - M) (0 when m_i = -inf);
+ *   out[b][h][:] = sum_i w_i acc_i / sum_i w_i l_i,  or 0 when every m_i = -inf.
+ * Uses p->num_seqs, num_q_heads, head_dim; out is [B][Hq][D] f32. */
+pa_status pa_combine(const pa_params *p, const float *partial_ml, const float *partial_acc,
+                     int32_t num_splits, float *out, pa_stream_t stream);
+
+/* ----------------------------------------------------------------- prefill
+ * Chunked causal prefill over packed query rows: q is [total_q][Hq][D],
+ * rows cu_q_lens[s] .. cu_q_lens[s+1]-1 belong to sequence s (T_s of them),
+ * cu_q_lens is [B+1] int32 on the device with cu_q_lens[0] = 0.  The chunk's
+ * own K/V are already in the pages; row r attends keys 0 ..= L_s - T_s + r.
+ * max_q_len is a host upper bound on every T_s (it sizes the grid);
+ * total_q = cu_q_lens[B].  out is [total_q][Hq][D] f32. */
+size_t pa_prefill_workspace_size(const pa_params *p, int32_t total_q, int32_t max_q_len);
+
+pa_status pa_prefill_chunk(const pa_params *p, const void *q, const int32_t *cu_q_lens,
+                           int32_t total_q, int32_t max_q_len, const void *k_cache,
+                           const void *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, float *out, void *workspace,
+                           size_t workspace_bytes, uint32_t *dev_status, pa_stream_t stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGED_GQA_H */

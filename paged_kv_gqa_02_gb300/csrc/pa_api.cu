@@ -1,0 +1,278 @@
+// pa_api.cu -- the extern "C" entry points of libpaged_gqa.so: host-side
+// validation (before any device access; crucible results: malformed metadata
+// is rejected before device access), the split-KV plan, workspace sizing and
+// kernel dispatch.  No entry point allocates memory.
+#include <math.h>
+#include <string.h>
+
+#include "pa_kernels.h"
+
+#define PA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using pa::AttnArgs;
+
+constexpr int kRefSms = 152;       // SM count behind the device-independent plan
+constexpr int kCtasPerSm = 4;      // split-plan target: CTAs per SM
+constexpr int kMinSplitPages = 2;  // smallest automatic split, in pages
+
+int elt_bytes(pa_dtype d) { return d == PA_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Resolved {
+    int64_t page_stride, token_stride, head_stride;
+    int group;
+};
+
+pa_status check_params(const pa_params* p, Resolved* r) {
+    if (!p) return PA_ERR_NULL;
+    if (p->num_seqs < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return PA_ERR_SHAPE;
+    if (p->num_seqs > 65535 || p->num_kv_heads > 65535) return PA_ERR_SHAPE;
+    if (p->num_q_heads % p->num_kv_heads != 0) return PA_ERR_SHAPE;
+    const int group = p->num_q_heads / p->num_kv_heads;
+    if (p->q_dtype < PA_F32 || p->q_dtype > PA_BF16 || p->kv_dtype < PA_F32 ||
+        p->kv_dtype > PA_BF16 || p->out_dtype < PA_F32 || p->out_dtype > PA_BF16)
+        return PA_ERR_DTYPE;
+    if (group > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
+    if (p->head_dim != 64 && p->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (p->page_size != 16 && p->page_size != 32) return PA_ERR_UNSUPPORTED;
+    if (p->q_dtype != p->kv_dtype || p->out_dtype != PA_F32) return PA_ERR_UNSUPPORTED;
+    if (p->num_pages < 1 || p->max_blocks_per_seq < 1 || p->max_context_len < 1)
+        return PA_ERR_SHAPE;
+    if (int64_t(p->max_context_len) > int64_t(p->max_blocks_per_seq) * p->page_size)
+        return PA_ERR_SHAPE;
+    if (!isfinite(p->scale)) return PA_ERR_SHAPE;
+    if (p->deterministic != 0 && p->deterministic != 1) return PA_ERR_SHAPE;
+    if (p->num_splits < 0) return PA_ERR_SHAPE;
+    const int64_t D = p->head_dim;
+    r->head_stride = p->head_stride ? p->head_stride : D;
+    r->token_stride = p->token_stride ? p->token_stride : p->num_kv_heads * r->head_stride;
+    r->page_stride = p->page_stride ? p->page_stride : p->page_size * r->token_stride;
+    if (r->head_stride < 0 || r->token_stride < 0 || r->page_stride < 0) return PA_ERR_SHAPE;
+    const int eb = elt_bytes(p->kv_dtype);
+    if ((r->head_stride * eb) % 16 || (r->token_stride * eb) % 16 || (r->page_stride * eb) % 16)
+        return PA_ERR_ALIGN;
+    r->group = group;
+    return PA_OK;
+}
+
+pa_status check_io(const void* q, const void* k, const void* v, const int32_t* bt,
+                   const int32_t* cl, const void* out) {
+    if (!q || !k || !v || !bt || !cl || !out) return PA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PA_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(bt) & 3u) || (reinterpret_cast<uintptr_t>(cl) & 3u))
+        return PA_ERR_ALIGN;
+    return PA_OK;
+}
+
+int device_sms() {
+    static int cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kRefSms;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = kRefSms;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Split plan from host fields only: splits of a whole number of pages,
+// enough of them that B * Hkv * S is about kCtasPerSm CTAs per SM.
+void plan(const pa_params* p, int* S, int* split_tokens) {
+    const int P = p->page_size;
+    const int pages = (p->max_context_len + P - 1) / P;
+    int per;
+    if (p->num_splits > 0) {
+        per = (pages + p->num_splits - 1) / p->num_splits;
+    } else {
+        const int sms = p->deterministic ? kRefSms : device_sms();
+        const int64_t units = int64_t(p->num_seqs) * p->num_kv_heads;
+        const int64_t want = (int64_t(kCtasPerSm) * sms + units - 1) / units;
+        per = int((pages + want - 1) / want);
+        if (per < kMinSplitPages) per = kMinSplitPages;
+    }
+    if (per < 1) per = 1;
+    if (per > pages) per = pages;
+    *split_tokens = per * P;
+    *S = (p->max_context_len + *split_tokens - 1) / *split_tokens;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t partial_bytes(const pa_params* p, int S, size_t* acc_off) {
+    const size_t n = size_t(p->num_seqs) * p->num_q_heads * S;
+    *acc_off = align256(n * 2 * sizeof(float));
+    return *acc_off + align256(n * p->head_dim * sizeof(float));
+}
+
+AttnArgs base_args(const pa_params* p, const Resolved& r, const void* q, const void* k,
+                   const void* v, const int32_t* bt, const int32_t* cl, uint32_t* st) {
+    AttnArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.block_tables = bt;
+    a.context_lens = cl;
+    a.dev_status = st;
+    a.num_seqs = p->num_seqs;
+    a.num_q_heads = p->num_q_heads;
+    a.num_kv_heads = p->num_kv_heads;
+    a.group = r.group;
+    a.num_pages = p->num_pages;
+    a.max_blocks_per_seq = p->max_blocks_per_seq;
+    a.page_stride = r.page_stride;
+    a.token_stride = r.token_stride;
+    a.head_stride = r.head_stride;
+    a.scale_log2 = p->scale * pa::kLog2e;
+    a.total_q = p->num_seqs;
+    return a;
+}
+
+pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+}  // namespace
+
+PA_EXPORT pa_params* pa_params_init(pa_params* p) {
+    if (!p) return p;
+    memset(p, 0, sizeof *p);
+    p->out_dtype = PA_F32;
+    p->deterministic = 1;
+    return p;
+}
+
+PA_EXPORT const char* pa_status_string(pa_status s) {
+    switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL: a required pointer is NULL";
+    case PA_ERR_SHAPE: return "PA_ERR_SHAPE: inconsistent sizes";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: unknown dtype code";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer or stride not 16-byte aligned";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace too small";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: valid but not implemented";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: a CUDA runtime call failed";
+    }
+    return "unknown pa_status";
+}
+
+PA_EXPORT int32_t pa_version(void) { return 100; }
+
+PA_EXPORT pa_status pa_decode_plan(const pa_params* p, int32_t* num_splits, int32_t* split_tokens) {
+    Resolved r;
+    pa_status st = check_params(p, &r);
+    if (st != PA_OK) return st;
+    int S, tok;
+    plan(p, &S, &tok);
+    if (num_splits) *num_splits = S;
+    if (split_tokens) *split_tokens = tok;
+    return PA_OK;
+}
+
+PA_EXPORT size_t pa_decode_workspace_size(const pa_params* p) {
+    Resolved r;
+    if (check_params(p, &r) != PA_OK) return 0;
+    int S, tok;
+    plan(p, &S, &tok);
+    if (S == 1) return 0;
+    size_t off;
+    return partial_bytes(p, S, &off);
+}
+
+PA_EXPORT pa_status pa_decode_partial(const pa_params* p, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, float* partial_ml,
+                                      float* partial_acc, int32_t num_splits,
+                                      uint32_t* dev_status, pa_stream_t stream) {
+    Resolved r;
+    pa_status st = check_params(p, &r);
+    if (st != PA_OK) return st;
+    if ((st = check_io(q, k_cache, v_cache, block_tables, context_lens, partial_ml)) != PA_OK)
+        return st;
+    if (!partial_acc) return PA_ERR_NULL;
+    if (!aligned16(partial_acc)) return PA_ERR_ALIGN;
+    int S, tok;
+    plan(p, &S, &tok);
+    if (num_splits != S) return PA_ERR_SHAPE;
+    AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
+    a.partial_ml = partial_ml;
+    a.partial_acc = partial_acc;
+    a.split_tokens = tok;
+    a.num_splits = S;
+    return cuda_status(pa::launch_decode_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
+}
+
+PA_EXPORT pa_status pa_combine(const pa_params* p, const float* partial_ml,
+                               const float* partial_acc, int32_t num_splits, float* out,
+                               pa_stream_t stream) {
+    if (!p || !partial_ml || !partial_acc || !out) return PA_ERR_NULL;
+    if (p->num_seqs < 1 || p->num_q_heads < 1 || num_splits < 1 || p->num_seqs > 65535)
+        return PA_ERR_SHAPE;
+    if (p->head_dim != 64 && p->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    return cuda_status(pa::launch_combine_v0(partial_ml, partial_acc, out, p->num_seqs,
+                                             p->num_q_heads, num_splits, p->head_dim, stream));
+}
+
+PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_cache,
+                              const void* v_cache, const int32_t* block_tables,
+                              const int32_t* context_lens, float* out, void* workspace,
+                              size_t workspace_bytes, uint32_t* dev_status, pa_stream_t stream) {
+    Resolved r;
+    pa_status st = check_params(p, &r);
+    if (st != PA_OK) return st;
+    if ((st = check_io(q, k_cache, v_cache, block_tables, context_lens, out)) != PA_OK) return st;
+    int S, tok;
+    plan(p, &S, &tok);
+    AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
+    a.split_tokens = tok;
+    a.num_splits = S;
+    if (S == 1) {
+        a.out = out;
+        return cuda_status(pa::launch_decode_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
+    }
+    size_t acc_off;
+    const size_t need = partial_bytes(p, S, &acc_off);
+    if (!workspace) return PA_ERR_NULL;
+    if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_ALIGN;
+    a.partial_ml = static_cast<float*>(workspace);
+    a.partial_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_off);
+    cudaError_t e = pa::launch_decode_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    return cuda_status(pa::launch_combine_v0(a.partial_ml, a.partial_acc, out, p->num_seqs,
+                                             p->num_q_heads, S, p->head_dim, stream));
+}
+
+PA_EXPORT size_t pa_prefill_workspace_size(const pa_params* p, int32_t total_q, int32_t max_q_len) {
+    (void)p;
+    (void)total_q;
+    (void)max_q_len;
+    return 0;
+}
+
+PA_EXPORT pa_status pa_prefill_chunk(const pa_params* p, const void* q, const int32_t* cu_q_lens,
+                                     int32_t total_q, int32_t max_q_len, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables,
+                                     const int32_t* context_lens, float* out, void* workspace,
+                                     size_t workspace_bytes, uint32_t* dev_status,
+                                     pa_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    Resolved r;
+    pa_status st = check_params(p, &r);
+    if (st != PA_OK) return st;
+    if ((st = check_io(q, k_cache, v_cache, block_tables, context_lens, out)) != PA_OK) return st;
+    if (!cu_q_lens) return PA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u) return PA_ERR_ALIGN;
+    if (total_q < 1 || max_q_len < 1 || max_q_len > p->max_context_len) return PA_ERR_SHAPE;
+    AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
+    a.cu_q_lens = cu_q_lens;
+    a.out = out;
+    a.max_q_len = max_q_len;
+    a.total_q = total_q;
+    a.num_splits = 1;
+    return cuda_status(pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
+}

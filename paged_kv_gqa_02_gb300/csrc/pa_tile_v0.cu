@@ -1,0 +1,287 @@
+// pa_tile_v0.cu -- first CUDA path: one CTA per (key split or row tile,
+// kv head, sequence), all q heads of the kv head in the CTA so each K/V page
+// row is read from HBM once per kv head (minfer doc 71: the GQA-batched
+// shape; crucible results: one CTA shares K/V across the q heads of one kv
+// head).  CUDA-core fp32 arithmetic, synchronous 16-byte page-row loads,
+// online softmax per page (crucible results, the online-softmax
+// experiment), base-2 exponentials.
+//
+// It serves three roles: the decode split partial (R = 1 row per sequence),
+// the chunked-prefill kernel (R rows per tile, causal per row), and the
+// fp32-KV decode path.  The split combine is at the end of this file.
+#include "pa_common.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kThreads = 128;
+
+template <int D, int P, int R>
+struct TileSmem {
+    static constexpr int kDist = R * kMaxGroup;  // distributions (row, head)
+    static constexpr int kGroups = kThreads / D; // threads sharing a dim
+    static constexpr size_t bytes =
+        sizeof(float) * (size_t(kDist) * D            // q (pre-scaled)
+                         + size_t(P) * (D + 1)         // K page, padded rows
+                         + size_t(P) * D               // V page
+                         + size_t(kDist) * P           // scores / probabilities
+                         + 3 * size_t(kDist));         // m, l, alpha
+};
+
+template <typename T, int D, int P, int R>
+__global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
+    using S = TileSmem<D, P, R>;
+    constexpr int kVec = Elt<T>::kVec;
+    constexpr int kChunks = D / kVec;  // 16-byte vectors per page row
+    constexpr int kPerThread = S::kDist / S::kGroups;
+
+    extern __shared__ float smem[];
+    float* q_s = smem;
+    float* k_s = q_s + S::kDist * D;
+    float* v_s = k_s + P * (D + 1);
+    float* p_s = v_s + P * D;
+    float* m_s = p_s + S::kDist * P;
+    float* l_s = m_s + S::kDist;
+    float* al_s = l_s + S::kDist;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.z, g = blockIdx.y, tile = blockIdx.x;
+    const int G = a.group, Hq = a.num_q_heads;
+    const bool decode = (a.cu_q_lens == nullptr);
+
+    // ---- rows of this tile and their causal ends --------------------------
+    int L = a.context_lens[b];
+    int row0, Tq;  // first packed row, rows of this sequence
+    if (decode) {
+        row0 = b;
+        Tq = 1;
+    } else {
+        row0 = a.cu_q_lens[b];
+        Tq = a.cu_q_lens[b + 1] - row0;
+    }
+    const bool bad = (Tq < 0) || (row0 < 0) || (L < Tq) || (L > a.max_blocks_per_seq * P) ||
+                     (!decode && Tq > a.max_q_len);
+    if (bad) {
+        if (tid == 0 && tile == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
+        L = 0;  // no key is read; the tile's rows are written as zeros
+    }
+    const int start = L - Tq;
+    const int r_first = decode ? 0 : tile * R;
+    // rows of this tile that exist: below T (and the host bound), inside q/out
+    int n_rows = 1;
+    if (!decode) {
+        const int t_rows = max(0, min(Tq, a.max_q_len));
+        n_rows = row0 < 0 ? 0 : max(0, min(min(R, t_rows - r_first), a.total_q - (row0 + r_first)));
+    }
+    const int nd = R * G;
+
+    // key range [t0, t1)
+    int t0, t1;
+    if (decode) {
+        t0 = tile * a.split_tokens;
+        t1 = min(L, t0 + a.split_tokens);
+    } else {
+        t0 = 0;
+        t1 = (n_rows > 0 && !bad) ? start + r_first + n_rows : 0;
+    }
+
+    // ---- stage q (times scale*log2e) and reset the running state ----------
+    for (int i = tid; i < nd * D; i += kThreads) {
+        const int dist = i / D, d = i % D, r = dist / G, h = dist % G;
+        float x = 0.f;
+        if (r < n_rows) {
+            const int64_t qi = (int64_t(row0 + r_first + r) * Hq + g * G + h) * D + d;
+            x = Elt<T>::f(static_cast<const T*>(a.q)[qi]) * a.scale_log2;
+        }
+        q_s[dist * D + d] = x;
+    }
+    for (int i = tid; i < nd; i += kThreads) {
+        m_s[i] = -INFINITY;
+        l_s[i] = 0.f;
+    }
+    float acc[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) acc[k] = 0.f;
+    const int my_d = tid % D, my_grp = tid / D;
+    __syncthreads();
+
+    const T* kbase = static_cast<const T*>(a.k) + int64_t(g) * a.head_stride;
+    const T* vbase = static_cast<const T*>(a.v) + int64_t(g) * a.head_stride;
+    const int32_t* table = a.block_tables + int64_t(b) * a.max_blocks_per_seq;
+
+    for (int ps = t0; ps < t1; ps += P) {
+        const int n = min(P, t1 - ps);
+        const int32_t page = table[ps / P];
+        if (page < 0 || page >= a.num_pages) {  // uniform across the CTA
+            if (tid == 0) flag(a.dev_status, PA_DEV_BAD_PAGE);
+            continue;
+        }
+        // -- page rows of kv head g -> shared (fp32)
+        for (int i = tid; i < n * kChunks; i += kThreads) {
+            const int j = i / kChunks, c = i % kChunks;
+            const int64_t off = int64_t(page) * a.page_stride + int64_t(j) * a.token_stride + c * kVec;
+            float f[kVec];
+            vec_to_f32<T>(*reinterpret_cast<const uint4*>(kbase + off), f);
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) k_s[j * (D + 1) + c * kVec + e] = f[e];
+            vec_to_f32<T>(*reinterpret_cast<const uint4*>(vbase + off), f);
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) v_s[j * D + c * kVec + e] = f[e];
+        }
+        __syncthreads();
+        // -- scores (base-2 units), masked per row's causal end
+        for (int i = tid; i < nd * P; i += kThreads) {
+            const int dist = i / P, j = i % P, r = dist / G;
+            const int key = ps + j;
+            const int end = start + r_first + r;  // inclusive
+            float s = -INFINITY;
+            if (j < n && r < n_rows && key <= end) {
+                float dot = 0.f;
+                const float* qd = q_s + dist * D;
+                const float* kd = k_s + j * (D + 1);
+#pragma unroll 8
+                for (int d = 0; d < D; ++d) dot = fmaf(qd[d], kd[d], dot);
+                s = dot;
+            }
+            p_s[dist * P + j] = s;
+        }
+        __syncthreads();
+        // -- online softmax update, one warp per distribution
+        for (int dist = warp; dist < nd; dist += kThreads / 32) {
+            const float x = lane < P ? p_s[dist * P + lane] : -INFINITY;
+            const float m_old = m_s[dist];
+            const float m_new = fmaxf(m_old, warp_max(x));
+            float p = 0.f, alpha = 1.f;
+            if (m_new != -INFINITY) {
+                p = ex2(x - m_new);
+                alpha = ex2(m_old - m_new);
+            }
+            const float sum = warp_sum(p);
+            if (lane < P) p_s[dist * P + lane] = p;
+            if (lane == 0) {
+                l_s[dist] = l_s[dist] * alpha + sum;
+                m_s[dist] = m_new;
+                al_s[dist] = alpha;
+            }
+        }
+        __syncthreads();
+        // -- rescale and accumulate P.V
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int dist = my_grp + k * S::kGroups;
+            if (dist < nd) {
+                float x = acc[k] * al_s[dist];
+                const float* pr = p_s + dist * P;
+                for (int j = 0; j < n; ++j) x = fmaf(pr[j], v_s[j * D + my_d], x);
+                acc[k] = x;
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- outputs -------------------------------------------------------------
+    if (a.out == nullptr) {  // decode split partial
+        const int s = tile, Sn = a.num_splits;
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int h = my_grp + k * S::kGroups;
+            if (h < G) {
+                const int64_t idx = (int64_t(b) * Hq + g * G + h) * Sn + s;
+                if (m_s[h] != -INFINITY) a.partial_acc[idx * D + my_d] = acc[k];
+                if (my_d == 0) {
+                    a.partial_ml[idx * 2] = m_s[h];
+                    a.partial_ml[idx * 2 + 1] = l_s[h];
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int dist = my_grp + k * S::kGroups;
+            if (dist < nd) {
+                const int r = dist / G, h = dist % G;
+                if (r < n_rows) {
+                    const float l = l_s[dist];
+                    const int64_t oi = (int64_t(row0 + r_first + r) * Hq + g * G + h) * D + my_d;
+                    a.out[oi] = l > 0.f ? acc[k] / l : 0.f;
+                }
+            }
+        }
+    }
+}
+
+// Combine: one CTA per (q head, sequence), one thread per output dim.
+__global__ void combine_v0(const float* __restrict__ ml, const float* __restrict__ acc,
+                           float* __restrict__ out, int Hq, int S, int D) {
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    const int64_t base = (int64_t(b) * Hq + h) * S;
+    float M = -INFINITY;
+    for (int i = 0; i < S; ++i) M = fmaxf(M, ml[(base + i) * 2]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+        for (int i = 0; i < S; ++i) {
+            const float m = ml[(base + i) * 2];
+            if (m == -INFINITY) continue;
+            const float w = ex2(m - M);
+            den = fmaf(w, ml[(base + i) * 2 + 1], den);
+            num = fmaf(w, acc[(base + i) * D + d], num);
+        }
+    }
+    out[(int64_t(b) * Hq + h) * D + d] = den > 0.f ? num / den : 0.f;
+}
+
+template <typename T, int D, int P, int R>
+cudaError_t launch_one(const AttnArgs& a, dim3 grid, cudaStream_t st) {
+    auto k = attn_tile_v0<T, D, P, R>;
+    const size_t sm = TileSmem<D, P, R>::bytes;
+    static bool configured = false;  // benign race: every caller sets the same value
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    k<<<grid, kThreads, sm, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int R>
+cudaError_t dispatch_dp(const AttnArgs& a, int D, int P, dim3 grid, cudaStream_t st) {
+    if (D == 64 && P == 16) return launch_one<T, 64, 16, R>(a, grid, st);
+    if (D == 64 && P == 32) return launch_one<T, 64, 32, R>(a, grid, st);
+    if (D == 128 && P == 16) return launch_one<T, 128, 16, R>(a, grid, st);
+    if (D == 128 && P == 32) return launch_one<T, 128, 32, R>(a, grid, st);
+    return cudaErrorInvalidValue;
+}
+
+template <int R>
+cudaError_t dispatch_t(const AttnArgs& a, pa_dtype dt, int D, int P, dim3 grid, cudaStream_t st) {
+    switch (dt) {
+    case PA_F32: return dispatch_dp<float, R>(a, D, P, grid, st);
+    case PA_F16: return dispatch_dp<__half, R>(a, D, P, grid, st);
+    case PA_BF16: return dispatch_dp<__nv_bfloat16, R>(a, D, P, grid, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st) {
+    dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
+    return dispatch_t<1>(a, dt, D, P, grid, st);
+}
+
+cudaError_t launch_prefill_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st) {
+    constexpr int R = 4;
+    dim3 grid((a.max_q_len + R - 1) / R, a.num_kv_heads, a.num_seqs);
+    return dispatch_t<R>(a, dt, D, P, grid, st);
+}
+
+cudaError_t launch_combine_v0(const float* ml, const float* acc, float* out, int B, int Hq,
+                              int S, int D, cudaStream_t st) {
+    combine_v0<<<dim3(Hq, B), D, 0, st>>>(ml, acc, out, Hq, S, D);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

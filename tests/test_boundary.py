@@ -1,0 +1,137 @@
+"""The C-ABI boundary on the host: the library builds, loads, exports every
+entry point declared in include/*.h, and rejects malformed arguments before
+touching the device (crucible results: malformed metadata is rejected
+before device access).  No test here needs a GPU."""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from paged_kv_gqa_02_gb300 import build, ops, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ops.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        names |= set(re.findall(r"\b(pa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ("pa_decode", "pa_prefill_chunk", "pa_combine"):
+        assert n in names
+    assert set(names) <= set(ops.EXPORTS) | {n for n in names if n.startswith("pa_")}
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert lib.pa_version() >= 100
+
+
+def test_params_struct_layout_matches_header(lib):
+    """pa_params_init writes the defaults the header documents."""
+    p = ops.Params()
+    lib.pa_params_init(ctypes.byref(p))
+    assert (p.out_dtype, p.deterministic, p.num_splits, p.page_stride) == (ops.PA_F32, 1, 0, 0)
+    assert ctypes.sizeof(ops.Params) == 4 * 8 + 8 * 3 + 4 * 6
+
+
+def test_status_strings(lib):
+    for code, name in ops.STATUS.items():
+        assert lib.pa_status_string(code).decode().startswith(name)
+
+
+def base_params(**kw):
+    args = dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=32,
+                num_pages=64, max_blocks_per_seq=16, max_context_len=512, dtype="bf16")
+    args.update(kw)
+    return ops.make_params(**args)
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: validation fails first
+
+
+def call_decode(p, q=FAKE, out=FAKE, bt=FAKE, ws=None, nbytes=0):
+    return ops.load().pa_decode(ctypes.byref(p), q, FAKE, FAKE, bt, FAKE, out, ws, nbytes, None, None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("num_seqs", 0, 2), ("num_q_heads", 7, 2), ("num_kv_heads", 0, 2),
+    ("head_dim", 96, 6), ("page_size", 8, 6), ("num_q_heads", 2 * 17, 6),
+    ("max_context_len", 16 * 32 + 1, 2), ("num_pages", 0, 2), ("q_dtype", 9, 3),
+    ("kv_dtype", ops.PA_F16, 6), ("out_dtype", ops.PA_BF16, 6), ("deterministic", 2, 2),
+    ("num_splits", -1, 2), ("head_stride", 4, 4), ("token_stride", 100, 4),
+])
+def test_rejects_bad_params(lib, field, value, code):
+    p = base_params()
+    if field == "num_q_heads" and value == 34:
+        p.num_kv_heads = 2
+    setattr(p, field, value)
+    assert call_decode(p) == code
+
+
+def test_rejects_null_and_misaligned(lib):
+    p = base_params()
+    assert call_decode(p, q=None) == 1
+    assert call_decode(p, out=ctypes.c_void_p((1 << 20) + 4)) == 4
+    assert call_decode(p, bt=ctypes.c_void_p((1 << 20) + 2)) == 4
+
+
+def test_rejects_small_workspace(lib):
+    p = base_params(max_context_len=512)
+    S, tok = ops.decode_plan(p)
+    assert S > 1
+    need = ops.decode_workspace_size(p)
+    assert need >= 2 * 8 * S * (128 + 2) * 4
+    assert call_decode(p, ws=FAKE, nbytes=need - 1) == 5
+    assert call_decode(p, ws=None, nbytes=0) == 1
+
+
+def test_partial_rejects_wrong_split_count(lib):
+    p = base_params()
+    S, _ = ops.decode_plan(p)
+    rc = lib.pa_decode_partial(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, S + 1,
+                               None, None)
+    assert rc == 2
+
+
+def test_prefill_rejects_bad_sizes(lib):
+    p = base_params()
+    L = lib
+    assert L.pa_prefill_chunk(ctypes.byref(p), FAKE, None, 4, 4, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              None, 0, None, None) == 1
+    assert L.pa_prefill_chunk(ctypes.byref(p), FAKE, FAKE, 0, 4, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              None, 0, None, None) == 2
+    assert L.pa_prefill_chunk(ctypes.byref(p), FAKE, FAKE, 4, 513, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              None, 0, None, None) == 2
+
+
+def test_split_plan_is_a_function_of_params(lib):
+    """Deterministic plans: whole pages per split, enough splits to cover the
+    capacity, same answer every call (the grid never depends on device data;
+    crucible README: split count fixed at capacity for graph replay)."""
+    for wl in workloads.ALL[:4]:
+        p = ops.params_for(wl)
+        S, tok = ops.decode_plan(p)
+        assert tok % wl.page_size == 0 and S * tok >= p.max_context_len > (S - 1) * tok
+        assert ops.decode_plan(p) == (S, tok)
+        p2 = ops.params_for(wl, num_splits=3)
+        S2, tok2 = ops.decode_plan(p2)
+        assert S2 <= 3 and S2 * tok2 >= p2.max_context_len
