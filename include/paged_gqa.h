@@ -155,6 +155,36 @@ pa_status pa_decode_partial(const pa_params *p, const void *q, const void *k_cac
 pa_status pa_combine(const pa_params *p, const float *partial_ml, const float *partial_acc,
                      int32_t num_splits, float *out, pa_stream_t stream);
 
+/* Decode without a workspace argument (the pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory at call
+ * time, such as an engine plugin whose host owns all device buffers, a
+ * serving loop that forbids allocation after start-up, or a process whose
+ * caching allocator already holds the free memory).
+ *
+ * It computes exactly what pa_decode computes, with the same kernels, but
+ * keeps the split partials in a static device array of
+ * PA_NOALLOC_SCRATCH_BYTES inside the library.  Every GPU that loads the
+ * library holds that array until the process exits.  It allocates nothing
+ * and calls no allocating routine.
+ *  - Limit: when the plan's partials (B * Hq * S * (D + 2) floats, each part
+ *    rounded up to 256 bytes) exceed PA_NOALLOC_SCRATCH_BYTES it returns
+ *    PA_ERR_WORKSPACE and launches nothing; use pa_decode with a workspace
+ *    or request fewer splits (pa_params.num_splits).
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress, with that device current).  Make that
+ *    first call before capturing any stream into a CUDA graph.
+ *  - Sharing: every call on a device uses the same array and leaves its
+ *    contents behind.  Nothing needs to start at zero (each call rewrites
+ *    every value it later reads), but calls whose kernels overlap on the
+ *    GPU (other streams, other host threads) race on the array: order them
+ *    on one stream or serialise them. */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+pa_status pa_decode_noalloc(const pa_params *p, const void *q, const void *k_cache,
+                            const void *v_cache, const int32_t *block_tables,
+                            const int32_t *context_lens, float *out, uint32_t *dev_status,
+                            pa_stream_t stream);
+
 /* ----------------------------------------------------------------- prefill
  * Chunked causal prefill over packed query rows: q is [total_q][Hq][D],
  * rows cu_q_lens[s] .. cu_q_lens[s+1]-1 belong to sequence s (T_s of them),

@@ -212,3 +212,22 @@ def device_inputs(inp, wl_or_dtype, device="cuda"):
                 block_tables=to_device(inp["block_tables"], None, device),
                 context_lens=to_device(inp["context_lens"], None, device),
                 cu_q_lens=to_device(inp["cu_q_lens"], None, device))
+
+
+def decode_noalloc(p: Params, q, k_cache, v_cache, block_tables, context_lens, out=None,
+                   dev_status=None, stream=None):
+    """pa_decode_noalloc: decode with the split partials in the library's
+    static device scratch (for callers that cannot allocate at call time).
+    Raises PaError(PA_ERR_WORKSPACE) when the partials exceed the scratch."""
+    L = load()
+    fn = L.pa_decode_noalloc
+    if fn.restype is not ctypes.c_int:
+        vp = ctypes.c_void_p
+        fn.argtypes = [ctypes.POINTER(Params), vp, vp, vp, vp, vp, vp, vp, vp]
+        fn.restype = ctypes.c_int
+    if out is None:
+        out = _empty_out(q, p)
+    _check(fn(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+              _ptr(context_lens), _ptr(out), _ptr(dev_status), _stream(stream)),
+           "pa_decode_noalloc")
+    return out
