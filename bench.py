@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ncu-once", action="store_true",
+                    help="profiling target: warm-up calls then one call of --workload, no graphs")
     return ap.parse_args()
 
 
@@ -256,22 +258,19 @@ def time_graph(torch, calls, K, W, world):
 
 
 def decode_calls(rot, ops, torch, partial_only=False):
-    p = rot.params
+    """pa_decode calls over the rotation copies; with partial_only, the same
+    calls restricted to the partial kernel (decode_phases = 1)."""
+    import copy
+    p = copy.copy(rot.params)
+    p.decode_phases = 1 if partial_only else 0
     S, _ = ops.decode_plan(p)
     nws = ops.decode_workspace_size(p)
     ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
-    ml = torch.empty((p.num_seqs, p.num_q_heads, S, 2), dtype=torch.float32, device="cuda")
-    acc = torch.empty((p.num_seqs, p.num_q_heads, S, p.head_dim), dtype=torch.float32, device="cuda")
-    calls = []
-    for i in range(rot.R):
-        if partial_only:
-            calls.append(lambda s, i=i: ops.decode_partial(p, rot.q[i], rot.k, rot.v, rot.bt[i], rot.cl,
-                                                           ml, acc, S, stream=s))
-        else:
-            calls.append(lambda s, i=i: ops.decode(p, rot.q[i], rot.k, rot.v, rot.bt[i], rot.cl,
-                                                   out=rot.out, workspace=ws if nws else None,
-                                                   stream=s))
-    launches = 1 if S == 1 or partial_only else 2
+    calls = [lambda s, i=i: ops.decode(p, rot.q[i], rot.k, rot.v, rot.bt[i], rot.cl, out=rot.out,
+                                       workspace=ws if nws else None, stream=s)
+             for i in range(rot.R)]
+    two_kernels = p.num_splits == 0 and p.kv_dtype != ops.PA_F32 or S > 1
+    launches = 1 if partial_only or not two_kernels else 2
     return calls, launches, S
 
 
@@ -525,9 +524,32 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_ncu_once(args):
+    """A short, graph-free run for ncu: `warmup` calls, then one call, on a
+    single copy of the inputs (ncu flushes caches between replays itself)."""
+    import torch
+    from paged_kv_gqa_02_gb300 import build, ops, workloads
+    build.build()
+    wl = workloads.BY_NAME[args.workload]
+    inp = wl.make_inputs()
+    d = ops.device_inputs(inp, wl)
+    p = ops.params_for(wl)
+    out = torch.empty((wl.total_q, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup + 1):
+        if wl.kind == "decode":
+            ops.decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], out=out)
+        else:
+            ops.prefill_chunk(p, d["q"], d["cu_q_lens"], wl.total_q, max(wl.q_lens), d["k_cache"],
+                              d["v_cache"], d["block_tables"], d["context_lens"], out=out)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_once": wl.name, "calls": args.warmup + 1}))
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.ncu_once:
+        run_ncu_once(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -95,6 +95,10 @@ typedef struct {
     pa_dtype out_dtype;         /* PA_F32                                      */
     int32_t deterministic;      /* 1: split plan from pa_params alone           */
     int32_t num_splits;         /* decode: 0 = automatic, else requested count  */
+    int32_t decode_phases;      /* pa_decode: 0 = both phases; 1 = partial step
+                                   only; 2 = combine step only (run after a
+                                   phase-1 call on the same workspace, to put
+                                   other work between the two or time them)     */
 } pa_params;
 
 /* Fills *p with defaults: contiguous strides, PA_F32 out, automatic splits,
@@ -119,13 +123,22 @@ const char *pa_status_string(pa_status s);
  * *split_tokens = keys per split.  Either output may be NULL. */
 pa_status pa_decode_plan(const pa_params *p, int32_t *num_splits, int32_t *split_tokens);
 
-/* Bytes of workspace pa_decode needs (0 when the plan has a single split).
- * Returns 0 for invalid parameters. */
+/* Bytes of workspace pa_decode needs for these parameters (0 on the fixed
+ * split path when the plan has a single split).  Returns 0 for invalid
+ * parameters. */
 size_t pa_decode_workspace_size(const pa_params *p);
 
-/* Decode attention: the split partials (when S > 1) and their combine.
+/* Decode attention: the split partials and their combine.
  * workspace: device memory of at least pa_decode_workspace_size(p) bytes,
- * 256-byte aligned, contents ignored.  dev_status may be NULL. */
+ * 256-byte aligned, contents ignored.  dev_status may be NULL.
+ *
+ * With num_splits = 0 and 16-bit K/V the partition is length-balanced: one
+ * persistent CTA per SM (a fixed 152 when deterministic = 1, the device's
+ * SM count otherwise) takes an equal contiguous share of the ordered
+ * (sequence, kv head, page) list; units that fall inside one CTA are
+ * finished there, the pieces of the others are merged by a second kernel in
+ * ascending CTA order.  Otherwise the fixed split plan of pa_decode_plan is
+ * used (the pa_decode_partial + pa_combine pair). */
 pa_status pa_decode(const pa_params *p, const void *q, const void *k_cache,
                     const void *v_cache, const int32_t *block_tables,
                     const int32_t *context_lens, float *out, void *workspace,

@@ -46,6 +46,7 @@ pa_status check_params(const pa_params* p, Resolved* r) {
     if (!isfinite(p->scale)) return PA_ERR_SHAPE;
     if (p->deterministic != 0 && p->deterministic != 1) return PA_ERR_SHAPE;
     if (p->num_splits < 0) return PA_ERR_SHAPE;
+    if (p->decode_phases < 0 || p->decode_phases > 3) return PA_ERR_SHAPE;
     const int64_t D = p->head_dim;
     r->head_stride = p->head_stride ? p->head_stride : D;
     r->token_stride = p->token_stride ? p->token_stride : p->num_kv_heads * r->head_stride;
@@ -102,6 +103,12 @@ void plan(const pa_params* p, int* S, int* split_tokens) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// pa_decode takes the length-balanced v1 path for 16-bit K/V unless a split
+// count is requested; it needs one persistent CTA per (reference) SM.
+bool use_v1(const pa_params* p) { return p->num_splits == 0 && p->kv_dtype != PA_F32; }
+
+int v1_ctas(const pa_params* p) { return p->deterministic ? kRefSms : device_sms(); }
 
 size_t partial_bytes(const pa_params* p, int S, size_t* acc_off) {
     const size_t n = size_t(p->num_seqs) * p->num_q_heads * S;
@@ -175,6 +182,9 @@ PA_EXPORT pa_status pa_decode_plan(const pa_params* p, int32_t* num_splits, int3
 PA_EXPORT size_t pa_decode_workspace_size(const pa_params* p) {
     Resolved r;
     if (check_params(p, &r) != PA_OK) return 0;
+    if (use_v1(p))
+        return pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads, p->num_kv_heads,
+                                             p->head_dim, v1_ctas(p));
     int S, tok;
     plan(p, &S, &tok);
     if (S == 1) return 0;
@@ -224,6 +234,39 @@ PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_c
     pa_status st = check_params(p, &r);
     if (st != PA_OK) return st;
     if ((st = check_io(q, k_cache, v_cache, block_tables, context_lens, out)) != PA_OK) return st;
+    if (use_v1(p)) {
+        const int n = v1_ctas(p);
+        const size_t need = pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads,
+                                                          p->num_kv_heads, p->head_dim, n);
+        if (!workspace) return PA_ERR_NULL;
+        if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_ALIGN;
+        pa::DecodeV1Call c;
+        c.q = q;
+        c.k = k_cache;
+        c.v = v_cache;
+        c.block_tables = block_tables;
+        c.context_lens = context_lens;
+        c.out = out;
+        c.workspace = workspace;
+        c.dev_status = dev_status;
+        c.dtype = p->kv_dtype;
+        c.B = p->num_seqs;
+        c.Hq = p->num_q_heads;
+        c.Hkv = p->num_kv_heads;
+        c.D = p->head_dim;
+        c.P = p->page_size;
+        c.num_pages = p->num_pages;
+        c.max_blocks = p->max_blocks_per_seq;
+        c.n_ctas = n;
+        c.page_stride = r.page_stride;
+        c.token_stride = r.token_stride;
+        c.head_stride = r.head_stride;
+        c.scale_log2 = p->scale * pa::kLog2e;
+        c.phases = p->decode_phases ? p->decode_phases : 3;
+        return cuda_status(pa::launch_decode_v1(c, stream));
+    }
+    const int phases = p->decode_phases ? p->decode_phases : 3;
     int S, tok;
     plan(p, &S, &tok);
     AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
@@ -231,6 +274,7 @@ PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_c
     a.num_splits = S;
     if (S == 1) {
         a.out = out;
+        if (!(phases & 1)) return PA_OK;
         return cuda_status(pa::launch_decode_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
     }
     size_t acc_off;
@@ -240,8 +284,11 @@ PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_c
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_ALIGN;
     a.partial_ml = static_cast<float*>(workspace);
     a.partial_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_off);
-    cudaError_t e = pa::launch_decode_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream);
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (phases & 1) {
+        cudaError_t e = pa::launch_decode_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (!(phases & 2)) return PA_OK;
     return cuda_status(pa::launch_combine_v0(a.partial_ml, a.partial_acc, out, p->num_seqs,
                                              p->num_q_heads, S, p->head_dim, stream));
 }

@@ -1,0 +1,724 @@
+// pa_decode_v1.cu -- decode attention for 16-bit K/V on sm_103a.
+//
+// Work partition (split-KV, crucible README "Split-position attention";
+// minfer doc 71: all q heads of a kv head share each K/V tile).  The work of
+// a call is the ordered list of (sequence, kv head) units, unit (b, g) made of
+// the pages of sequence b read for kv head g.  In a cost space where each
+// unit occupies unit_cost + pages positions (unit_cost stands for the fixed
+// work of a unit piece: its query rows and its result), the grid's
+// n = min(CTAs x 8 warps, T / kMinPartCost) parts take equal contiguous shares
+// [v*T/n, (v+1)*T/n).  Every warp therefore moves about the same
+// number of bytes whatever the mix of context lengths, and the grid does not
+// depend on device data.  A warp finishes a unit that lies inside its share;
+// the pieces of the other units go to the workspace and a combine kernel,
+// launched with programmatic dependent launch, merges them in ascending part
+// order.
+//
+// Each warp reads the block table of its share ahead (32 pages at a time,
+// one lane per page) and issues its own TMA copies of each page's K and V
+// tiles (one kv head, all page_size slots, 128B-swizzled) into its own ring
+// of half-stages guarded by mbarriers, refilling a slot as soon as it has
+// used it; no warp waits for another.  Each warp streams its pages: S = Q K^T with
+// mma.sync m16n8k16 (the group's q heads padded to 16 rows), an online softmax
+// in base 2 (crucible results, the online-softmax experiment), and O += P V
+// with m16n8k16 whose A operand is built from the S accumulator in registers.
+// The probabilities are split into a 16-bit high part and a 16-bit remainder
+// stacked along k (the V fragment is passed twice), keeping 16 (bf16) or 22
+// (f16) bits of them: one 16-bit rounding alone moves small outputs by more
+// than 1% of their size.
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "pa_common.cuh"
+#include "pa_kernels.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kCW = 8;                        // warps per CTA, each a partition part
+constexpr int kThreadsV1 = kCW * 32;
+constexpr uint32_t kWaitLimit = 1u << 22;     // polls before a wait gives up
+constexpr int kMaxHalf = 8;                   // half-stages per warp ring, at most
+constexpr int kSmemLimit = 232448;            // 227 KiB opt-in per CTA
+constexpr int kUnitCost = 2;                  // partition weight of a unit piece, in pages
+constexpr int kMinPartCost = 4;               // smallest share worth a warp, in cost units
+
+struct V1Params {
+    const void* q;  // [B*Hq][D]
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* out;
+    float* ws_ml;   // [slot][G][2]
+    float* ws_acc;  // [slot][G][D]
+    uint32_t* dev_status;
+    int32_t B, Hq, Hkv, G, num_pages, max_blocks, max_len;
+    float scale_log2;
+    int32_t n_parts, nhs, head_first, unit_cost;
+};
+
+// A warp's position in its share of the cost space.
+struct Walk {
+    long long start, s, e;  // cost position of the unit's first slot; share [s, e)
+    int b, g, pb, pf, pe;   // unit, its pages, the pages [pf, pe) of it in the share
+    int done;
+};
+
+__host__ __device__ inline size_t v1_fixed_bytes() {
+    return size_t(kCW) * kMaxHalf * 4      // page id of each half-stage
+           + size_t(kCW) * kMaxHalf * 8;   // a full barrier per half-stage
+}
+
+__device__ inline int pages_of_len(int L, int P, int max_len) {
+    return (L >= 1 && L <= max_len) ? (L + P - 1) / P : 0;
+}
+
+__device__ inline int seq_pages(const int32_t* cl, int b, int P, int max_len) {
+    return pages_of_len(__ldg(cl + b), P, max_len);
+}
+
+__device__ inline long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ inline long long warp_incl_scan_ll(long long v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// Total cost T of the call (all units with pages).  Whole warp.
+__device__ inline long long total_cost(const V1Params& a, int P) {
+    long long tot = 0;
+    for (int b = threadIdx.x & 31; b < a.B; b += 32) {
+        const int pb = seq_pages(a.context_lens, b, P, a.max_len);
+        if (pb > 0) tot += (long long)a.Hkv * (pb + a.unit_cost);
+    }
+    return warp_sum_ll(tot);
+}
+
+// The walk of share [s, e): its first unit piece.  Whole warp.
+__device__ inline Walk walk_start(const V1Params& a, int P, long long s, long long e) {
+    const int lane = threadIdx.x & 31, W = a.unit_cost;
+    Walk w{0, s, e, 0, 0, 0, 0, 0, 1};
+    if (e <= s) return w;
+    long long basep = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int pb = b < a.B ? seq_pages(a.context_lens, b, P, a.max_len) : 0;
+        const long long c = pb > 0 ? (long long)a.Hkv * (pb + W) : 0;
+        const long long incl = warp_incl_scan_ll(c, lane);
+        const long long total = __shfl_sync(0xffffffffu, incl, 31);
+        if (s < basep + total) {
+            const unsigned m = __ballot_sync(0xffffffffu, basep + incl > s);
+            const int j = __ffs(m) - 1;
+            const long long seq0 = basep + __shfl_sync(0xffffffffu, incl - c, j);
+            w.pb = __shfl_sync(0xffffffffu, pb, j);
+            w.b = b0 + j;
+            w.g = int((s - seq0) / (w.pb + W));
+            w.start = seq0 + (long long)w.g * (w.pb + W);
+            const long long pf = s - w.start - W > 0 ? s - w.start - W : 0;
+            const long long room = e - w.start - W;
+            const long long pe = room < w.pb ? room : w.pb;
+            w.pf = int(pf);
+            w.pe = int(pe);
+            w.done = pe <= pf;
+            return w;
+        }
+        basep += total;
+    }
+    return w;
+}
+
+// Moves to the next unit with pages; done once its pages start at or after e.
+__device__ inline void walk_next_unit(Walk& w, const V1Params& a, int P) {
+    w.start += w.pb + a.unit_cost;
+    if (++w.g == a.Hkv) {
+        w.g = 0;
+        int pb = 0;
+        do {
+            ++w.b;
+        } while (w.b < a.B && (pb = seq_pages(a.context_lens, w.b, P, a.max_len)) == 0);
+        if (w.b >= a.B) {
+            w.done = 1;
+            return;
+        }
+        w.pb = pb;
+    }
+    w.pf = 0;
+    const long long room = w.e - w.start - a.unit_cost;
+    w.pe = int(room < w.pb ? room : w.pb);
+    if (w.pe <= 0) w.done = 1;
+}
+
+// Advances the walk by j pages; `i` is the current page within the unit.
+__device__ inline void walk_advance(Walk& w, int& i, int j, const V1Params& a, int P) {
+    while (!w.done && j > 0) {
+        const int rem = w.pe - i;
+        if (j < rem) {
+            i += j;
+            j = 0;
+        } else {
+            j -= rem;
+            walk_next_unit(w, a, P);
+            i = w.pf;
+        }
+    }
+}
+
+// Splits two probabilities into 16-bit high parts and 16-bit remainders,
+// packed as the pairs an MMA A-fragment register holds.
+template <typename T>
+__device__ inline void split_hi_lo(float x, float y, uint32_t& hi, uint32_t& lo) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+        const float2 f = __bfloat1622float2(h);
+        const __nv_bfloat162 r = __floats2bfloat162_rn(x - f.x, y - f.y);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+        lo = *reinterpret_cast<const uint32_t*>(&r);
+    } else {
+        const __half2 h = __floats2half2_rn(x, y);
+        const float2 f = __half22float2(h);
+        const __half2 r = __floats2half2_rn(x - f.x, y - f.y);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+        lo = *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
+// Part v of the partition runs on CTA v % n_ctas, warp v / n_ctas, so that
+// when fewer parts than warps are in use every SM still gets a share.  The
+// number of parts in use is a function of the inputs alone.
+__device__ inline long long parts_in_use(long long T, const V1Params& a) {
+    const long long want = (T + kMinPartCost - 1) / kMinPartCost;
+    return want < 1 ? 1 : (want < a.n_parts ? want : a.n_parts);
+}
+
+// The load side of a warp: lane l holds page base + l of the warp's share
+// (its kv head, page id and whether it exists).
+struct LoadWindow {
+    Walk w;     // walk state at page `base` of the share
+    int i;      // page within the unit at `base`
+    int base;   // share page index of lane 0
+    int live, g, page;
+};
+
+__device__ inline void window_fill(LoadWindow& lw, const V1Params& a, int P) {
+    Walk x = lw.w;
+    int i = lw.i;
+    walk_advance(x, i, threadIdx.x & 31, a, P);
+    lw.live = x.done ? 0 : 1;
+    lw.g = x.g;
+    lw.page = lw.live ? __ldg(a.block_tables + (long long)x.b * a.max_blocks + i) : -1;
+}
+
+template <typename T, int D, int P>
+__global__ void __launch_bounds__(kThreadsV1, 1)
+    decode_v1(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const V1Params a) {
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int kHalves = D / 64;     // 128-byte swizzle spans per row
+    constexpr int kTile = P * D * 2;    // one K (or V) page tile: a half-stage
+    constexpr int kTb = P / 8;          // 8-token blocks per page
+    constexpr int kKs = D / 16;         // k-steps of Q K^T
+    constexpr int kNt = D / 8;          // n-tiles of P V
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const int NH = a.nhs;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* my_tiles = base + size_t(warp) * NH * kTile;  // [NH][kTile]
+    int* my_page = reinterpret_cast<int*>(base + size_t(kCW) * NH * kTile) + warp * kMaxHalf;
+    uint64_t* my_full =
+        reinterpret_cast<uint64_t*>(reinterpret_cast<int*>(base + size_t(kCW) * NH * kTile) + kCW * kMaxHalf) +
+        warp * kMaxHalf;
+
+    pdl_launch_dependents();
+
+    if (lane == 0) {
+        for (int s = 0; s < NH; ++s) mbar_init(&my_full[s], 1);
+        mbar_fence_init();
+        if (warp == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
+    }
+    __syncwarp();
+
+    // ---- this warp's share of the cost space ------------------------------------
+    const long long cost = total_cost(a, P);
+    const long long n_used = parts_in_use(cost, a);
+    const long long part = (long long)warp * gridDim.x + blockIdx.x;
+    if (part >= n_used) return;
+    Walk wk = walk_start(a, P, part * cost / n_used, (part + 1) * cost / n_used);
+    if (wk.done) return;
+
+    // ---- load side: issue half-stage x (page x/2 of the share; K, then V)
+    LoadWindow lw{wk, wk.pf, 0, 0, 0, -1};
+    window_fill(lw, a, P);
+    bool timed_out = false;
+    auto issue = [&](int hx) {
+        const int j = hx >> 1;
+        while (j >= lw.base + 32) {  // next 32 pages of the share
+            walk_advance(lw.w, lw.i, 32, a, P);
+            lw.base += 32;
+            window_fill(lw, a, P);
+        }
+        const int src = j - lw.base;
+        const int live = __shfl_sync(0xffffffffu, lw.live, src);
+        const int g = __shfl_sync(0xffffffffu, lw.g, src);
+        const int pg = __shfl_sync(0xffffffffu, lw.page, src);
+        if (!live) return;
+        if (lane == 0) {
+            const int slot = hx % NH;
+            const bool ok = pg >= 0 && pg < a.num_pages;
+            if (!ok && (hx & 1) == 0) flag(a.dev_status, PA_DEV_BAD_PAGE);
+            my_page[slot] = ok ? pg : -1;
+            mbar_arrive_expect_tx(&my_full[slot], ok ? kTile : 0);
+            if (ok) {
+                uint8_t* dst = my_tiles + size_t(slot) * kTile;
+                const int xc = a.head_first ? g : 0, yc = a.head_first ? 0 : g;
+#pragma unroll
+                for (int hh = 0; hh < kHalves; ++hh)
+                    tma_load_4d(dst + hh * P * 128, (hx & 1) ? &tmV : &tmK, &my_full[slot], 64 * hh, xc, yc,
+                                pg);
+            }
+        }
+        __syncwarp();
+    };
+    for (int hx = 0; hx < NH; ++hx) issue(hx);
+
+    // ---- compute side ---------------------------------------------------------------
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const int G = a.G;
+    // ldmatrix row addresses: lane supplies row (lane & 7) of matrix (lane >> 3);
+    // matrix m of a 32-dim block jj is the 16-byte chunk 4*jj + m (swizzled)
+    uint32_t koff[D / 32];
+#pragma unroll
+    for (int jj = 0; jj < D / 32; ++jj) {
+        const int chunk = 4 * jj + (lane >> 3), rr = lane & 7;
+        koff[jj] = (chunk >> 3) * (P * 128) + rr * 128 + (((chunk & 7) ^ rr) << 4);
+    }
+    uint32_t qf[kKs][4], qn[kKs][4];
+    float o[kNt][4];
+    float sc[kTb][4];
+    // query rows of unit (b, g) straight into A fragments (rows >= G are 0)
+    auto load_q = [&](uint32_t (&dst)[kKs][4], int b, int g) {
+        const T* qb = static_cast<const T*>(a.q) + ((long long)b * a.Hq + g * G) * D;
+#pragma unroll
+        for (int ks = 0; ks < kKs; ++ks) {
+            const int col = 16 * ks + 2 * t4;
+            dst[ks][0] = g4 < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + g4 * D + col)) : 0u;
+            dst[ks][1] = g4 + 8 < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + (g4 + 8) * D + col)) : 0u;
+            dst[ks][2] = g4 < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + g4 * D + col + 8)) : 0u;
+            dst[ks][3] = g4 + 8 < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + (g4 + 8) * D + col + 8)) : 0u;
+        }
+    };
+    load_q(qn, wk.b, wk.g);
+    int x = 0;  // half-stage number
+
+    while (!wk.done) {
+        const int L = __ldg(a.context_lens + wk.b);
+        const bool whole = (wk.pf == 0) && (wk.pe == wk.pb);
+#pragma unroll
+        for (int ks = 0; ks < kKs; ++ks)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qf[ks][e] = qn[ks][e];
+        Walk nx = wk;  // the next piece, whose query rows load now
+        walk_next_unit(nx, a, P);
+        if (!nx.done) load_q(qn, nx.b, nx.g);
+
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < kNt; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+        for (int i = wk.pf; i < wk.pe; ++i) {
+            const int ntok = min(P, L - i * P);
+            // ---- K tile: S = Q K^T, masked, online softmax
+            bool ok = !timed_out;
+            if (ok && !mbar_wait(&my_full[x % NH], (x / NH) & 1, kWaitLimit)) {
+                timed_out = true;
+                ok = false;
+                if (lane == 0) flag(a.dev_status, PA_DEV_TIMEOUT);
+            }
+            const bool valid = ok && my_page[x % NH] >= 0;
+            if (valid) {
+                const uint32_t kb = smem_u32(my_tiles + size_t(x % NH) * kTile);
+#pragma unroll
+                for (int tb = 0; tb < kTb; ++tb) sc[tb][0] = sc[tb][1] = sc[tb][2] = sc[tb][3] = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < D / 32; ++jj) {
+#pragma unroll
+                    for (int tb = 0; tb < kTb; ++tb) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kb + tb * 1024 + koff[jj], b0, b1, b2, b3);
+                        mma_16816<kBf>(sc[tb], qf[2 * jj], b0, b1);
+                        mma_16816<kBf>(sc[tb], qf[2 * jj + 1], b2, b3);
+                    }
+                }
+            }
+            __syncwarp();
+            if (!timed_out) issue(x + NH);  // the K slot is free again
+            ++x;
+            if (valid) {
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int tb = 0; tb < kTb; ++tb) {
+                    const int tok = tb * 8 + 2 * t4;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        sc[tb][e] *= a.scale_log2;
+                        if (tok + (e & 1) >= ntok) sc[tb][e] = -INFINITY;
+                    }
+                    mx0 = fmaxf(mx0, fmaxf(sc[tb][0], sc[tb][1]));
+                    mx1 = fmaxf(mx1, fmaxf(sc[tb][2], sc[tb][3]));
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);  // m = -inf -> 0
+                m0 = mn0;
+                m1 = mn1;
+                float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+                for (int tb = 0; tb < kTb; ++tb) {
+                    sc[tb][0] = ex2(sc[tb][0] - mn0);
+                    sc[tb][1] = ex2(sc[tb][1] - mn0);
+                    sc[tb][2] = ex2(sc[tb][2] - mn1);
+                    sc[tb][3] = ex2(sc[tb][3] - mn1);
+                    ps0 += sc[tb][0] + sc[tb][1];
+                    ps1 += sc[tb][2] + sc[tb][3];
+                }
+                l0 = l0 * al0 + ps0;
+                l1 = l1 * al1 + ps1;
+                if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
+#pragma unroll
+                    for (int nt = 0; nt < kNt; ++nt) {
+                        o[nt][0] *= al0;
+                        o[nt][1] *= al0;
+                        o[nt][2] *= al1;
+                        o[nt][3] *= al1;
+                    }
+                }
+            }
+            // ---- V tile: O += P V
+            ok = !timed_out;
+            if (ok && !mbar_wait(&my_full[x % NH], (x / NH) & 1, kWaitLimit)) {
+                timed_out = true;
+                ok = false;
+                if (lane == 0) flag(a.dev_status, PA_DEV_TIMEOUT);
+            }
+            if (valid && ok) {
+                uint8_t* vt = my_tiles + size_t(x % NH) * kTile;
+                if (ntok < P) {  // rows past the context hold arbitrary bits: zero them
+                    for (int y = lane; y < (P - ntok) * kHalves * 8; y += 32) {
+                        const int rowi = ntok + y / (kHalves * 8);
+                        const int rem = y % (kHalves * 8);
+                        *reinterpret_cast<uint4*>(vt + (rem >> 3) * (P * 128) + rowi * 128 + (rem & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                const uint32_t vb = smem_u32(vt);
+#pragma unroll
+                for (int tb = 0; tb < kTb; ++tb) {
+                    uint32_t pa[4];
+                    split_hi_lo<T>(sc[tb][0], sc[tb][1], pa[0], pa[2]);
+                    split_hi_lo<T>(sc[tb][2], sc[tb][3], pa[1], pa[3]);
+#pragma unroll
+                    for (int jj = 0; jj < D / 32; ++jj) {
+                        uint32_t v[4];
+                        ldsm_x4_t(vb + tb * 1024 + koff[jj], v[0], v[1], v[2], v[3]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) mma_16816<kBf>(o[4 * jj + q], pa, v[q], v[q]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (!timed_out) issue(x + NH);  // the V slot is free again
+            ++x;
+        }
+
+        // ---- the piece's result: final output, or a partial for the combine
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if (whole) {
+            const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+            float* ob = a.out + ((long long)wk.b * a.Hq + wk.g * G) * D;
+#pragma unroll
+            for (int nt = 0; nt < kNt; ++nt) {
+                const int col = nt * 8 + 2 * t4;
+                if (g4 < G)
+                    *reinterpret_cast<float2*>(ob + g4 * D + col) = make_float2(o[nt][0] * i0, o[nt][1] * i0);
+                if (g4 + 8 < G)
+                    *reinterpret_cast<float2*>(ob + (g4 + 8) * D + col) =
+                        make_float2(o[nt][2] * i1, o[nt][3] * i1);
+            }
+        } else {
+            const long long slot = part + (long long)wk.b * a.Hkv + wk.g;
+            float* accp = a.ws_acc + slot * G * D;
+            float* ml = a.ws_ml + slot * G * 2;
+#pragma unroll
+            for (int nt = 0; nt < kNt; ++nt) {
+                const int col = nt * 8 + 2 * t4;
+                if (g4 < G) *reinterpret_cast<float2*>(accp + g4 * D + col) = make_float2(o[nt][0], o[nt][1]);
+                if (g4 + 8 < G)
+                    *reinterpret_cast<float2*>(accp + (g4 + 8) * D + col) = make_float2(o[nt][2], o[nt][3]);
+            }
+            if (t4 == 0) {
+                if (g4 < G) *reinterpret_cast<float2*>(ml + g4 * 2) = make_float2(m0, l0);
+                if (g4 + 8 < G) *reinterpret_cast<float2*>(ml + (g4 + 8) * 2) = make_float2(m1, l1);
+            }
+        }
+        wk = nx;
+    }
+    // A wait that gave up may leave copies in flight: wait (bounded) for them.
+    if (timed_out && lane == 0)
+        for (int s = 0; s < NH; ++s) mbar_wait(&my_full[s], ((x + s) / NH) & 1, 1024);
+}
+
+// Merges the pieces of units that span several parts: one CTA per (q head,
+// sequence), one thread per output dim.  The pieces' maxima and weights are
+// spread over the threads and reduced by fixed shuffle trees, so the result
+// does not depend on timing.
+template <int D>
+__global__ void __launch_bounds__(D) combine_v1(const V1Params a, int P) {
+    extern __shared__ float wsh[];  // one weight per piece, up to n_parts + 1
+    __shared__ long long sh[2];
+    __shared__ float red[D / 32];
+    pdl_wait_primary();
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, wid = d >> 5;
+    const int g = h / a.G, r = h % a.G, unit = b * a.Hkv + g;
+    const int W = a.unit_cost;
+    if (threadIdx.x < 32) {
+        long long tot = 0, pre = 0;
+        for (int x = threadIdx.x; x < a.B; x += 32) {
+            const int pg = seq_pages(a.context_lens, x, P, a.max_len);
+            const long long cst = pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
+            tot += cst;
+            if (x < b) pre += cst;
+        }
+        tot = warp_sum_ll(tot);
+        pre = warp_sum_ll(pre);
+        if (threadIdx.x == 0) {
+            sh[0] = tot;
+            sh[1] = pre;
+        }
+    }
+    __syncthreads();
+    const long long T = sh[0];
+    const int pb = seq_pages(a.context_lens, b, P, a.max_len);
+    float* o = a.out + ((long long)b * a.Hq + h) * D;
+    if (pb == 0) {
+        o[d] = 0.f;
+        if (h == 0 && d == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
+        return;
+    }
+    // the unit's pages sit at cost positions [p0, p0 + pb); part v owns
+    // [v*T/n, (v+1)*T/n), so position x belongs to part ((x+1)*n - 1) / T
+    const long long n = parts_in_use(T, a);
+    const long long p0 = sh[1] + (long long)g * (pb + W) + W;
+    const int c0 = int(((p0 + 1) * n - 1) / T);
+    const int c1 = int(((p0 + pb) * n - 1) / T);
+    if (c0 == c1) return;  // finished inside one part
+    const int np = c1 - c0 + 1;
+    // pass 1: each piece's maximum (parts between c0 and c1 whose share is
+    // empty, possible when T < n, wrote nothing and are skipped)
+    float mloc = -INFINITY;
+    for (int x = d; x < np; x += D) {
+        const long long cc = c0 + x;
+        float m = -INFINITY;
+        if (cc * T / n != (cc + 1) * T / n) m = a.ws_ml[((cc + unit) * a.G + r) * 2];
+        wsh[x] = m;
+        mloc = fmaxf(mloc, m);
+    }
+    mloc = warp_max(mloc);
+    if (lane == 0) red[wid] = mloc;
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int y = 0; y < D / 32; ++y) M = fmaxf(M, red[y]);
+    __syncthreads();
+    // pass 2: weights 2^(m - M) and the denominator
+    float dloc = 0.f;
+    for (int x = d; x < np; x += D) {
+        const float m = wsh[x];
+        float wgt = 0.f;
+        if (m != -INFINITY) {
+            wgt = ex2(m - M);
+            dloc = fmaf(wgt, a.ws_ml[((long long)(c0 + x + unit) * a.G + r) * 2 + 1], dloc);
+        }
+        wsh[x] = wgt;
+    }
+    dloc = warp_sum(dloc);
+    if (lane == 0) red[wid] = dloc;
+    __syncthreads();
+    float den = 0.f;
+#pragma unroll
+    for (int y = 0; y < D / 32; ++y) den += red[y];
+    // pass 3: the weighted accumulators, independent loads in flight
+    const float* acc = a.ws_acc + ((long long)(c0 + unit) * a.G + r) * D + d;
+    const long long stride = (long long)a.G * D;
+    float num = 0.f;
+#pragma unroll 8
+    for (int x = 0; x < np; ++x) {
+        const float wgt = wsh[x];
+        if (wgt != 0.f) num = fmaf(wgt, acc[x * stride], num);
+    }
+    o[d] = den > 0.f ? num / den : 0.f;
+}
+
+// ---- host side -------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Half-stages per warp ring: as many K/V page tiles as shared memory holds.
+int half_stages(int D, int P) {
+    const size_t tile = size_t(P) * D * 2;
+    const size_t room = size_t(kSmemLimit) - 1024 - v1_fixed_bytes();
+    const int n = int(room / (kCW * tile));
+    return n > kMaxHalf ? kMaxHalf : n;
+}
+
+size_t smem_bytes(int D, int P, int nhs) {
+    return 1024 + size_t(kCW) * nhs * P * D * 2 + v1_fixed_bytes();
+}
+
+template <typename T, int D, int P>
+cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Params& a, int n_ctas,
+                         int phases, cudaStream_t st) {
+    if (phases & 1) {
+        auto kern = decode_v1<T, D, P>;
+        static bool configured = false;  // benign race: every caller sets the same value
+        if (!configured) {
+            cudaError_t e =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+            if (e != cudaSuccess) return e;
+            configured = true;
+        }
+        kern<<<n_ctas, kThreadsV1, smem_bytes(D, P, a.nhs), st>>>(k, v, a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (!(phases & 2)) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.Hq, a.B);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = sizeof(float) * size_t(a.n_parts + 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_v1<D>, a, P);
+}
+
+size_t ws_ml_bytes(size_t slots, size_t G) { return (slots * G * 2 * sizeof(float) + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t decode_v1_workspace_bytes(int B, int Hq, int Hkv, int D, int n_ctas) {
+    const size_t slots = size_t(n_ctas) * kCW + size_t(B) * Hkv;
+    const size_t G = size_t(Hq / Hkv);
+    return ws_ml_bytes(slots, G) + slots * G * D * sizeof(float);
+}
+
+cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int D = call.D, P = call.P;
+    const CUtensorMapDataType dt =
+        call.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // The pool as a 4-d tensor (head_dim, kv head, slot, page), the two middle
+    // dimensions in stride order; the box is one page of one kv head, 64 dims
+    // (128 bytes, the swizzle span) at a time.
+    const int head_first = call.head_stride <= call.token_stride;
+    CUtensorMap mk, mv;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+    dims[0] = D;
+    dims[3] = cuuint64_t(call.num_pages);
+    strides[2] = cuuint64_t(call.page_stride) * 2;
+    if (head_first) {
+        dims[1] = call.Hkv;
+        dims[2] = P;
+        strides[0] = cuuint64_t(call.head_stride) * 2;
+        strides[1] = cuuint64_t(call.token_stride) * 2;
+        box[0] = 64; box[1] = 1; box[2] = P; box[3] = 1;
+    } else {
+        dims[1] = P;
+        dims[2] = call.Hkv;
+        strides[0] = cuuint64_t(call.token_stride) * 2;
+        strides[1] = cuuint64_t(call.head_stride) * 2;
+        box[0] = 64; box[1] = P; box[2] = 1; box[3] = 1;
+    }
+    if (enc(&mk, dt, 4, const_cast<void*>(call.k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (enc(&mv, dt, 4, const_cast<void*>(call.v), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    V1Params a;
+    a.q = call.q;
+    a.block_tables = call.block_tables;
+    a.context_lens = call.context_lens;
+    a.out = call.out;
+    const int G = call.Hq / call.Hkv;
+    const size_t slots = size_t(call.n_ctas) * kCW + size_t(call.B) * call.Hkv;
+    a.ws_ml = static_cast<float*>(call.workspace);
+    a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(call.workspace) + ws_ml_bytes(slots, G));
+    a.dev_status = call.dev_status;
+    a.B = call.B;
+    a.Hq = call.Hq;
+    a.Hkv = call.Hkv;
+    a.G = G;
+    a.num_pages = call.num_pages;
+    a.max_blocks = call.max_blocks;
+    a.max_len = call.max_blocks * P;
+    a.scale_log2 = call.scale_log2;
+    a.n_parts = call.n_ctas * kCW;
+    a.nhs = half_stages(D, P);
+    a.head_first = head_first;
+    a.unit_cost = kUnitCost;
+    if (a.nhs < 2) return cudaErrorInvalidValue;
+    const bool bf = call.dtype == PA_BF16;
+#define PA_V1_CASE(DD, PP)                                                                        \
+    if (D == DD && P == PP)                                                                       \
+        return bf ? launch_typed<__nv_bfloat16, DD, PP>(mk, mv, a, call.n_ctas, call.phases, st) \
+                  : launch_typed<__half, DD, PP>(mk, mv, a, call.n_ctas, call.phases, st);
+    PA_V1_CASE(128, 32)
+    PA_V1_CASE(128, 16)
+    PA_V1_CASE(64, 32)
+    PA_V1_CASE(64, 16)
+#undef PA_V1_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

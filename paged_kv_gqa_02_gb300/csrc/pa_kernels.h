@@ -14,4 +14,24 @@ cudaError_t launch_prefill_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cuda
 cudaError_t launch_combine_v0(const float* ml, const float* acc, float* out, int B, int Hq,
                               int S, int D, cudaStream_t st);
 
+// v1 decode for 16-bit K/V: persistent length-balanced partial kernel (TMA +
+// mma.sync) followed by a PDL-launched combine of split units.
+struct DecodeV1Call {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* out;
+    void* workspace;  // decode_v1_workspace_bytes(...) bytes, 256-byte aligned
+    uint32_t* dev_status;
+    pa_dtype dtype;
+    int B, Hq, Hkv, D, P, num_pages, max_blocks, n_ctas;
+    int64_t page_stride, token_stride, head_stride;
+    float scale_log2;
+    int phases;  // bit 0: partial kernel, bit 1: combine kernel
+};
+size_t decode_v1_workspace_bytes(int B, int Hq, int Hkv, int D, int n_ctas);
+cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st);
+
 }  // namespace pa

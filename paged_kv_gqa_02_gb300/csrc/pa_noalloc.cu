@@ -52,9 +52,6 @@ PA_EXPORT pa_status pa_decode_noalloc(const pa_params* p, const void* q, const v
     int32_t S = 0, split_tokens = 0;
     pa_status st = pa_decode_plan(p, &S, &split_tokens);
     if (st != PA_OK) return st;
-    if (S == 1)  // a single split writes out directly and needs no scratch
-        return pa_decode(p, q, k_cache, v_cache, block_tables, context_lens, out, nullptr, 0,
-                         dev_status, stream);
     // partial layout: m/l pairs, then the 256-byte aligned accumulators
     const size_t n = size_t(p->num_seqs) * p->num_q_heads * S;
     const size_t acc_off = round256(n * 2 * sizeof(float));

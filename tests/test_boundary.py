@@ -50,7 +50,7 @@ def test_params_struct_layout_matches_header(lib):
     p = ops.Params()
     lib.pa_params_init(ctypes.byref(p))
     assert (p.out_dtype, p.deterministic, p.num_splits, p.page_stride) == (ops.PA_F32, 1, 0, 0)
-    assert ctypes.sizeof(ops.Params) == 4 * 8 + 8 * 3 + 4 * 6
+    assert ctypes.sizeof(ops.Params) == 4 * 8 + 8 * 3 + 4 * 8
 
 
 def test_status_strings(lib):
@@ -78,6 +78,7 @@ def call_decode(p, q=FAKE, out=FAKE, bt=FAKE, ws=None, nbytes=0):
     ("max_context_len", 16 * 32 + 1, 2), ("num_pages", 0, 2), ("q_dtype", 9, 3),
     ("kv_dtype", ops.PA_F16, 6), ("out_dtype", ops.PA_BF16, 6), ("deterministic", 2, 2),
     ("num_splits", -1, 2), ("head_stride", 4, 4), ("token_stride", 100, 4),
+    ("decode_phases", 4, 2), ("decode_phases", -1, 2),
 ])
 def test_rejects_bad_params(lib, field, value, code):
     p = base_params()

@@ -69,3 +69,18 @@ def test_noalloc_rejects_partials_beyond_the_scratch():
         ops.decode_noalloc(p, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                            d["context_lens"])
     assert e.value.code == 5
+
+
+def test_noalloc_single_split_plan():
+    """Short contexts plan a single split; the scratch still holds it."""
+    inp, meta = problem(B=4, Hq=16, Hkv=4, D=128, P=32, lens=(1, 17, 40, 64), dt="f16",
+                        num_pages=12, seed=17)
+    p = _params(inp, meta)
+    assert ops.decode_plan(p)[0] == 1
+    d = ops.device_inputs(inp, "f16")
+    got = ops.decode_noalloc(p, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"])
+    want = ops.decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"])
+    torch.cuda.synchronize()
+    assert_within(got.cpu().numpy(), want.cpu().numpy().astype(np.float64), workloads.TOL_16,
+                  "noalloc single split")
