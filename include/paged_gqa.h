@@ -95,8 +95,8 @@ typedef struct {
     pa_dtype out_dtype;         /* PA_F32                                      */
     int32_t deterministic;      /* 1: split plan from pa_params alone           */
     int32_t num_splits;         /* decode: 0 = automatic, else requested count  */
-    int32_t decode_phases;      /* pa_decode: 0 = both phases; 1 = partial step
-                                   only; 2 = combine step only (run after a
+    int32_t decode_phases;      /* pa_decode: 0 = both steps; 1 = partial step
+                                   only; 2 = combine step only (after a
                                    phase-1 call on the same workspace, to put
                                    other work between the two or time them)     */
 } pa_params;
@@ -134,11 +134,11 @@ size_t pa_decode_workspace_size(const pa_params *p);
  *
  * With num_splits = 0 and 16-bit K/V the partition is length-balanced: one
  * persistent CTA per SM (a fixed 152 when deterministic = 1, the device's
- * SM count otherwise) takes an equal contiguous share of the ordered
- * (sequence, kv head, page) list; units that fall inside one CTA are
- * finished there, the pieces of the others are merged by a second kernel in
- * ascending CTA order.  Otherwise the fixed split plan of pa_decode_plan is
- * used (the pa_decode_partial + pa_combine pair). */
+ * SM count otherwise; 8 warps each) takes equal contiguous shares of the
+ * ordered (sequence, kv head, page) list, each warp one share; units that
+ * fall inside one share are finished there, and a second kernel merges the
+ * pieces of the others in ascending share order.  Otherwise the fixed split
+ * plan of pa_decode_plan is used (the pa_decode_partial + pa_combine pair). */
 pa_status pa_decode(const pa_params *p, const void *q, const void *k_cache,
                     const void *v_cache, const int32_t *block_tables,
                     const int32_t *context_lens, float *out, void *workspace,

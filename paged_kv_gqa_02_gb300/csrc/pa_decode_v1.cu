@@ -12,7 +12,8 @@
 // depend on device data.  A warp finishes a unit that lies inside its share;
 // the pieces of the other units go to the workspace and a combine kernel,
 // launched with programmatic dependent launch, merges them in ascending part
-// order.
+// order (split-KV combine, crucible README "Split-position attention":
+// rescale by exp(m_i - m_max), then merge).
 //
 // Each warp reads the block table of its share ahead (32 pages at a time,
 // one lane per page) and issues its own TMA copies of each page's K and V
@@ -41,7 +42,8 @@ namespace {
 constexpr int kCW = 8;                        // warps per CTA, each a partition part
 constexpr int kThreadsV1 = kCW * 32;
 constexpr uint32_t kWaitLimit = 1u << 22;     // polls before a wait gives up
-constexpr int kMaxHalf = 8;                   // half-stages per warp ring, at most
+constexpr int kMaxTiles = 64;                 // page tiles (half-stages) per CTA, at most
+constexpr int kMaxRing = 6;                   // page tiles in one warp's ring, at most
 constexpr int kSmemLimit = 232448;            // 227 KiB opt-in per CTA
 constexpr int kUnitCost = 2;                  // partition weight of a unit piece, in pages
 constexpr int kMinPartCost = 4;               // smallest share worth a warp, in cost units
@@ -56,7 +58,7 @@ struct V1Params {
     uint32_t* dev_status;
     int32_t B, Hq, Hkv, G, num_pages, max_blocks, max_len;
     float scale_log2;
-    int32_t n_parts, nhs, head_first, unit_cost;
+    int32_t n_parts, ntiles, head_first, unit_cost;
 };
 
 // A warp's position in its share of the cost space.
@@ -67,8 +69,8 @@ struct Walk {
 };
 
 __host__ __device__ inline size_t v1_fixed_bytes() {
-    return size_t(kCW) * kMaxHalf * 4      // page id of each half-stage
-           + size_t(kCW) * kMaxHalf * 8;   // a full barrier per half-stage
+    return size_t(kMaxTiles) * 4      // page id of each tile
+           + size_t(kMaxTiles) * 8;   // a full barrier per tile
 }
 
 __device__ inline int pages_of_len(int L, int P, int max_len) {
@@ -218,8 +220,10 @@ __device__ inline void window_fill(LoadWindow& lw, const V1Params& a, int P) {
     lw.page = lw.live ? __ldg(a.block_tables + (long long)x.b * a.max_blocks + i) : -1;
 }
 
+// At most 224 registers a thread: 256 x 224 leaves room on the SM for one
+// combine CTA, which then starts (and locates its items) while this grid runs.
 template <typename T, int D, int P>
-__global__ void __launch_bounds__(kThreadsV1, 1)
+__global__ void __maxnreg__(224)
     decode_v1(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const V1Params a) {
     constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
@@ -232,16 +236,25 @@ __global__ void __launch_bounds__(kThreadsV1, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    const int NH = a.nhs;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t* my_tiles = base + size_t(warp) * NH * kTile;  // [NH][kTile]
-    int* my_page = reinterpret_cast<int*>(base + size_t(kCW) * NH * kTile) + warp * kMaxHalf;
-    uint64_t* my_full =
-        reinterpret_cast<uint64_t*>(reinterpret_cast<int*>(base + size_t(kCW) * NH * kTile) + kCW * kMaxHalf) +
-        warp * kMaxHalf;
 
     pdl_launch_dependents();
 
+    // ---- this warp's share of the cost space ------------------------------------
+    const long long cost = total_cost(a, P);
+    const long long n_used = parts_in_use(cost, a);
+    const long long part = (long long)warp * gridDim.x + blockIdx.x;
+    if (part >= n_used) return;
+    // The CTA's pool of page tiles is divided among its active warps
+    // (warps 0 .. active-1), so a CTA with few parts keeps more pages in
+    // flight per part.
+    const int active = int((n_used - blockIdx.x + gridDim.x - 1) / gridDim.x);
+    const int NH = min(a.ntiles / active, kMaxRing);
+    uint8_t* my_tiles = base + size_t(warp) * NH * kTile;  // [NH][kTile]
+    int* my_page = reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile) + warp * NH;
+    uint64_t* my_full =
+        reinterpret_cast<uint64_t*>(reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile) + kMaxTiles) +
+        warp * NH;
     if (lane == 0) {
         for (int s = 0; s < NH; ++s) mbar_init(&my_full[s], 1);
         mbar_fence_init();
@@ -251,12 +264,6 @@ __global__ void __launch_bounds__(kThreadsV1, 1)
         }
     }
     __syncwarp();
-
-    // ---- this warp's share of the cost space ------------------------------------
-    const long long cost = total_cost(a, P);
-    const long long n_used = parts_in_use(cost, a);
-    const long long part = (long long)warp * gridDim.x + blockIdx.x;
-    if (part >= n_used) return;
     Walk wk = walk_start(a, P, part * cost / n_used, (part + 1) * cost / n_used);
     if (wk.done) return;
 
@@ -293,7 +300,7 @@ __global__ void __launch_bounds__(kThreadsV1, 1)
         }
         __syncwarp();
     };
-    for (int hx = 0; hx < NH; ++hx) issue(hx);
+    for (int hx = 0; hx < NH; ++hx) issue(hx);  // fill the ring
 
     // ---- compute side ---------------------------------------------------------------
     const int g4 = lane >> 2, t4 = lane & 3;
@@ -489,95 +496,109 @@ __global__ void __launch_bounds__(kThreadsV1, 1)
         for (int s = 0; s < NH; ++s) mbar_wait(&my_full[s], ((x + s) / NH) & 1, 1024);
 }
 
-// Merges the pieces of units that span several parts: one CTA per (q head,
-// sequence), one thread per output dim.  The pieces' maxima and weights are
-// spread over the threads and reduced by fixed shuffle trees, so the result
-// does not depend on timing.
+// Merges the pieces of units that span several parts.  A persistent grid of
+// one CTA per SM, resident beside the partial kernel (which it waits for
+// through programmatic dependent launch), gives each warp (q head, sequence)
+// items in turn.  A warp locates an item's pieces from the lengths alone (a
+// lane-parallel prefix over the sequences before it) before the partial
+// kernel ends; only the pieces' loads come after.  The maxima and
+// denominators are reduced by fixed shuffle trees, so the result does not
+// depend on timing.  At most 64 registers a thread (D threads, 1024/D CTAs an
+// SM), so the CTA fits beside a partial CTA of 256 x 224 registers.
 template <int D>
-__global__ void __launch_bounds__(D) combine_v1(const V1Params a, int P) {
-    extern __shared__ float wsh[];  // one weight per piece, up to n_parts + 1
-    __shared__ long long sh[2];
-    __shared__ float red[D / 32];
-    pdl_wait_primary();
-    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, wid = d >> 5;
-    const int g = h / a.G, r = h % a.G, unit = b * a.Hkv + g;
+__global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int P) {
+    constexpr int kWarps = D / 32;
+    constexpr int kVpl = D / 32;  // output dims per lane
+    __shared__ long long sh_T;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int W = a.unit_cost;
-    if (threadIdx.x < 32) {
-        long long tot = 0, pre = 0;
-        for (int x = threadIdx.x; x < a.B; x += 32) {
+    const int n_items = a.Hq * a.B;
+    if (wid == 0) {
+        long long tot = 0;
+        for (int x = lane; x < a.B; x += 32) {
             const int pg = seq_pages(a.context_lens, x, P, a.max_len);
-            const long long cst = pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
-            tot += cst;
-            if (x < b) pre += cst;
+            tot += pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
         }
         tot = warp_sum_ll(tot);
+        if (lane == 0) sh_T = tot;
+    }
+    __syncthreads();
+    const long long T = sh_T;
+    const long long n = parts_in_use(T > 0 ? T : 1, a);
+    bool waited = false;
+    for (int it = blockIdx.x * kWarps + wid; it < n_items; it += gridDim.x * kWarps) {
+        const int b = it / a.Hq, h = it % a.Hq, g = h / a.G, r = h % a.G;
+        const int unit = b * a.Hkv + g;
+        // ---- locate the item's pieces
+        long long pre = 0;
+        for (int x = lane; x < b; x += 32) {
+            const int pg = seq_pages(a.context_lens, x, P, a.max_len);
+            pre += pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
+        }
         pre = warp_sum_ll(pre);
-        if (threadIdx.x == 0) {
-            sh[0] = tot;
-            sh[1] = pre;
+        const int pb = seq_pages(a.context_lens, b, P, a.max_len);
+        int c0 = 0, np = 0;
+        if (pb > 0) {  // the unit's pages sit at cost positions [p0, p0 + pb)
+            const long long p0 = pre + (long long)g * (pb + W) + W;
+            c0 = int(((p0 + 1) * n - 1) / T);  // part v owns [v*T/n, (v+1)*T/n)
+            const int c1 = int(((p0 + pb) * n - 1) / T);
+            np = c1 > c0 ? c1 - c0 + 1 : 0;  // 0: finished inside one part
         }
-    }
-    __syncthreads();
-    const long long T = sh[0];
-    const int pb = seq_pages(a.context_lens, b, P, a.max_len);
-    float* o = a.out + ((long long)b * a.Hq + h) * D;
-    if (pb == 0) {
-        o[d] = 0.f;
-        if (h == 0 && d == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
-        return;
-    }
-    // the unit's pages sit at cost positions [p0, p0 + pb); part v owns
-    // [v*T/n, (v+1)*T/n), so position x belongs to part ((x+1)*n - 1) / T
-    const long long n = parts_in_use(T, a);
-    const long long p0 = sh[1] + (long long)g * (pb + W) + W;
-    const int c0 = int(((p0 + 1) * n - 1) / T);
-    const int c1 = int(((p0 + pb) * n - 1) / T);
-    if (c0 == c1) return;  // finished inside one part
-    const int np = c1 - c0 + 1;
-    // pass 1: each piece's maximum (parts between c0 and c1 whose share is
-    // empty, possible when T < n, wrote nothing and are skipped)
-    float mloc = -INFINITY;
-    for (int x = d; x < np; x += D) {
-        const long long cc = c0 + x;
-        float m = -INFINITY;
-        if (cc * T / n != (cc + 1) * T / n) m = a.ws_ml[((cc + unit) * a.G + r) * 2];
-        wsh[x] = m;
-        mloc = fmaxf(mloc, m);
-    }
-    mloc = warp_max(mloc);
-    if (lane == 0) red[wid] = mloc;
-    __syncthreads();
-    float M = -INFINITY;
-#pragma unroll
-    for (int y = 0; y < D / 32; ++y) M = fmaxf(M, red[y]);
-    __syncthreads();
-    // pass 2: weights 2^(m - M) and the denominator
-    float dloc = 0.f;
-    for (int x = d; x < np; x += D) {
-        const float m = wsh[x];
-        float wgt = 0.f;
-        if (m != -INFINITY) {
-            wgt = ex2(m - M);
-            dloc = fmaf(wgt, a.ws_ml[((long long)(c0 + x + unit) * a.G + r) * 2 + 1], dloc);
+        if (!waited) {  // the partial kernel's pieces are complete from here on
+            pdl_wait_primary();
+            waited = true;
         }
-        wsh[x] = wgt;
-    }
-    dloc = warp_sum(dloc);
-    if (lane == 0) red[wid] = dloc;
-    __syncthreads();
-    float den = 0.f;
+        float* o = a.out + ((long long)b * a.Hq + h) * D + lane * kVpl;
+        if (pb == 0) {
 #pragma unroll
-    for (int y = 0; y < D / 32; ++y) den += red[y];
-    // pass 3: the weighted accumulators, independent loads in flight
-    const float* acc = a.ws_acc + ((long long)(c0 + unit) * a.G + r) * D + d;
-    const long long stride = (long long)a.G * D;
-    float num = 0.f;
+            for (int e = 0; e < kVpl; ++e) o[e] = 0.f;
+            if (h == 0 && lane == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
+            continue;
+        }
+        if (np == 0) continue;
+        // ---- merge; parts between c0 and c1 whose share is empty (possible when
+        // T < n) wrote nothing: their weight is 0 and their rows are never used
+        float M = -INFINITY;
+        for (int x = lane; x < np; x += 32) {
+            const long long cc = c0 + x;
+            if (cc * T / n != (cc + 1) * T / n) M = fmaxf(M, a.ws_ml[((cc + unit) * a.G + r) * 2]);
+        }
+        M = warp_max(M);
+        float den = 0.f, num[kVpl];
+#pragma unroll
+        for (int e = 0; e < kVpl; ++e) num[e] = 0.f;
+        for (int x0 = 0; x0 < np; x0 += 32) {
+            const long long cc = c0 + x0 + lane;
+            float wgt = 0.f;
+            if (x0 + lane < np && cc * T / n != (cc + 1) * T / n) {
+                const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((cc + unit) * a.G + r) * 2);
+                if (ml.x != -INFINITY) {
+                    wgt = ex2(ml.x - M);
+                    den = fmaf(wgt, ml.y, den);
+                }
+            }
+            const int cnt = min(32, np - x0);
+            const float* accp = a.ws_acc + ((long long)(c0 + x0 + unit) * a.G + r) * D + lane * kVpl;
 #pragma unroll 8
-    for (int x = 0; x < np; ++x) {
-        const float wgt = wsh[x];
-        if (wgt != 0.f) num = fmaf(wgt, acc[x * stride], num);
+            for (int j = 0; j < cnt; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, wgt, j);
+                float v[kVpl];
+                if constexpr (kVpl == 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(accp + (long long)j * a.G * D);
+                    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2*>(accp + (long long)j * a.G * D);
+                    v[0] = t.x; v[1] = t.y;
+                }
+#pragma unroll
+                for (int e = 0; e < kVpl; ++e) num[e] = wj != 0.f ? fmaf(wj, v[e], num[e]) : num[e];
+            }
+        }
+        den = warp_sum(den);
+#pragma unroll
+        for (int e = 0; e < kVpl; ++e) o[e] = den > 0.f ? num[e] / den : 0.f;
     }
-    o[d] = den > 0.f ? num / den : 0.f;
+    if (!waited) pdl_wait_primary();
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -595,16 +616,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Half-stages per warp ring: as many K/V page tiles as shared memory holds.
-int half_stages(int D, int P) {
+// Page tiles per CTA: as many K/V page tiles as shared memory holds once a
+// combine CTA (static shared memory and the per-CTA reservation) has room.
+int tile_count(int D, int P) {
     const size_t tile = size_t(P) * D * 2;
-    const size_t room = size_t(kSmemLimit) - 1024 - v1_fixed_bytes();
-    const int n = int(room / (kCW * tile));
-    return n > kMaxHalf ? kMaxHalf : n;
+    const size_t room = size_t(kSmemLimit) - 1024 - v1_fixed_bytes() - 2048;
+    const int n = int(room / tile);
+    return n > kMaxTiles ? kMaxTiles : n;
 }
 
-size_t smem_bytes(int D, int P, int nhs) {
-    return 1024 + size_t(kCW) * nhs * P * D * 2 + v1_fixed_bytes();
+size_t smem_bytes(int D, int P, int ntiles) {
+    return 1024 + size_t(ntiles) * P * D * 2 + v1_fixed_bytes();
 }
 
 template <typename T, int D, int P>
@@ -619,15 +641,14 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
             if (e != cudaSuccess) return e;
             configured = true;
         }
-        kern<<<n_ctas, kThreadsV1, smem_bytes(D, P, a.nhs), st>>>(k, v, a);
+        kern<<<n_ctas, kThreadsV1, smem_bytes(D, P, a.ntiles), st>>>(k, v, a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (!(phases & 2)) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.Hq, a.B);
+    cfg.gridDim = dim3(n_ctas);
     cfg.blockDim = dim3(D);
-    cfg.dynamicSmemBytes = sizeof(float) * size_t(a.n_parts + 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -637,14 +658,26 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
     return cudaLaunchKernelEx(&cfg, combine_v1<D>, a, P);
 }
 
-size_t ws_ml_bytes(size_t slots, size_t G) { return (slots * G * 2 * sizeof(float) + 255) & ~size_t(255); }
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace: (m, l) pairs, then accumulators, one slot per (part, unit) piece.
+struct WsLayout {
+    size_t ml, acc, total;
+};
+WsLayout ws_layout(int B, int Hq, int Hkv, int D, int n_ctas) {
+    const size_t slots = size_t(n_ctas) * kCW + size_t(B) * Hkv;
+    const size_t G = size_t(Hq / Hkv);
+    WsLayout w;
+    w.ml = 0;
+    w.acc = w.ml + round256(slots * G * 2 * sizeof(float));
+    w.total = w.acc + slots * G * D * sizeof(float);
+    return w;
+}
 
 }  // namespace
 
 size_t decode_v1_workspace_bytes(int B, int Hq, int Hkv, int D, int n_ctas) {
-    const size_t slots = size_t(n_ctas) * kCW + size_t(B) * Hkv;
-    const size_t G = size_t(Hq / Hkv);
-    return ws_ml_bytes(slots, G) + slots * G * D * sizeof(float);
+    return ws_layout(B, Hq, Hkv, D, n_ctas).total;
 }
 
 cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
@@ -691,9 +724,10 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.context_lens = call.context_lens;
     a.out = call.out;
     const int G = call.Hq / call.Hkv;
-    const size_t slots = size_t(call.n_ctas) * kCW + size_t(call.B) * call.Hkv;
-    a.ws_ml = static_cast<float*>(call.workspace);
-    a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(call.workspace) + ws_ml_bytes(slots, G));
+    const WsLayout wl = ws_layout(call.B, call.Hq, call.Hkv, D, call.n_ctas);
+    char* ws = static_cast<char*>(call.workspace);
+    a.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
+    a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
     a.dev_status = call.dev_status;
     a.B = call.B;
     a.Hq = call.Hq;
@@ -704,10 +738,10 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.max_len = call.max_blocks * P;
     a.scale_log2 = call.scale_log2;
     a.n_parts = call.n_ctas * kCW;
-    a.nhs = half_stages(D, P);
+    a.ntiles = tile_count(D, P);
     a.head_first = head_first;
     a.unit_cost = kUnitCost;
-    if (a.nhs < 2) return cudaErrorInvalidValue;
+    if (a.ntiles < 2 * kCW) return cudaErrorInvalidValue;
     const bool bf = call.dtype == PA_BF16;
 #define PA_V1_CASE(DD, PP)                                                                        \
     if (D == DD && P == PP)                                                                       \

@@ -75,6 +75,15 @@ __device__ inline void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* 
         : "memory");
 }
 
+// Pulls a tile of a tensor into L2 ahead of use (no shared memory, no barrier).
+__device__ inline void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 __device__ inline void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

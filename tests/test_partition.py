@@ -1,56 +1,85 @@
 """Host-side model of the length-balanced decode partition.
 
-CTA c of n owns positions [c*T/n, (c+1)*T/n) of the ordered (sequence, kv
-head, page) list; the combine finds a unit's owners as
-c(x) = ((x + 1) * n - 1) // T and skips CTAs whose share is empty.  These
-properties are what the partial and combine kernels rely on."""
+Cost space: unit (sequence b, kv head g) with pb > 0 pages occupies W + pb
+positions (W for the fixed work of a unit piece, then its pages); n parts
+(at most one per warp, fewer when the total cost T is small) own
+[v*T/n, (v+1)*T/n).  A part walks the units its share meets and processes the
+pages whose positions fall inside it.  The combine locates a unit's pieces
+as the parts between owner(first page) and owner(last page) whose share is
+not empty, owner(x) = ((x + 1) * n - 1) // T.  These are the properties the
+partial and combine kernels rely on."""
 from __future__ import annotations
 
 import numpy as np
 import pytest
 
+MIN_PART_COST = 4
 
-def share(c, T, n):
-    return c * T // n, (c + 1) * T // n
+
+def parts_in_use(T, n_parts):
+    return max(1, min(n_parts, (T + MIN_PART_COST - 1) // MIN_PART_COST))
 
 
 def owner(x, T, n):
     return ((x + 1) * n - 1) // T
 
 
-@pytest.mark.parametrize("seed", range(40))
-def test_owners_and_pieces(seed):
+def walk(share, units, W):
+    """Pieces (unit index, first page, end page) of a share, walking the units
+    like the kernel: start at the unit holding position share[0]."""
+    s, e = share
+    pieces = []
+    for u, (start, pb) in enumerate(units):
+        if pb == 0:
+            continue
+        pf = max(0, s - start - W)
+        pe = min(pb, e - start - W)
+        if pe > pf:
+            pieces.append((u, pf, pe))
+    return pieces
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_cost_partition(seed):
     rng = np.random.default_rng(seed)
-    B = int(rng.integers(1, 20))
+    B = int(rng.integers(1, 24))
     Hkv = int(rng.integers(1, 9))
-    n = int(rng.choice([1, 7, 148, 152, 160]))
-    pages = [int(x) for x in rng.integers(0, 40, size=B)]
-    T = Hkv * sum(pages)
-    if T == 0:
-        return
-    # every position has exactly one owner, and owner() finds it
-    own = np.full(T, -1)
-    for c in range(n):
-        a, b = share(c, T, n)
-        assert a <= b
-        own[a:b] = c
-    assert (own >= 0).all()
-    assert all(owner(x, T, n) == own[x] for x in range(T))
-    # pieces of each unit: the non-empty CTAs between its first and last owner
-    start = 0
-    slots = set()
+    W = 2
+    n_parts = int(rng.choice([8, 56, 1216]))
+    pages = [int(x) for x in rng.integers(0, 60, size=B)]
+    pages = [p if rng.random() > 0.1 else 0 for p in pages]  # some invalid lengths
+    units, start = [], 0
     for b in range(B):
         for g in range(Hkv):
-            s_u, e_u = start, start + pages[b]
-            start = e_u
-            if pages[b] == 0:
-                continue
-            c0, c1 = owner(s_u, T, n), owner(e_u - 1, T, n)
-            pieces = [c for c in range(c0, c1 + 1) if share(c, T, n)[0] < share(c, T, n)[1]]
-            touching = sorted({own[x] for x in range(s_u, e_u)})
-            assert pieces == touching
-            u = b * Hkv + g
-            for c in pieces:  # workspace slot c + u is unique
-                assert (c + u) not in slots
-                slots.add(c + u)
-                assert c + u < n + B * Hkv
+            units.append((start, pages[b]))
+            if pages[b]:
+                start += W + pages[b]
+    T = start
+    if T == 0:
+        return
+    n = parts_in_use(T, n_parts)
+    assert 1 <= n <= n_parts
+    shares = [(v * T // n, (v + 1) * T // n) for v in range(n)]
+    covered = {}
+    slots = set()
+    per_unit = {}
+    for v, sh in enumerate(shares):
+        for (u, pf, pe) in walk(sh, units, W):
+            for i in range(pf, pe):
+                assert (u, i) not in covered, "page processed twice"
+                covered[(u, i)] = v
+            per_unit.setdefault(u, []).append((v, pf, pe))
+            assert v + u < n_parts + len(units) and (v + u) not in slots
+            slots.add(v + u)
+    for u, (ustart, pb) in enumerate(units):
+        if pb == 0:
+            assert u not in per_unit
+            continue
+        assert all((u, i) in covered for i in range(pb)), "page never processed"
+        p0 = ustart + W
+        c0, c1 = owner(p0, T, n), owner(p0 + pb - 1, T, n)
+        want = [v for v in range(c0, c1 + 1) if shares[v][0] < shares[v][1]]
+        got = [v for v, _, _ in per_unit[u]]
+        assert got == want
+        whole = [(pf == 0 and pe == pb) for _, pf, pe in per_unit[u]]
+        assert any(whole) == (c0 == c1) == (len(got) == 1)
