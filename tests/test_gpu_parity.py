@@ -114,6 +114,14 @@ PREFILL_CASES = [
     (3, 16, 2, 128, 32, (300, 64, 33), (9, 64, 1), "bf16"),
     (2, 64, 8, 128, 32, (160, 96), (96, 32), "bf16"),
     (4, 28, 4, 128, 32, (17, 64, 129, 257), (17, 64, 129, 257), "f16"),
+    # tensor-core path: every group size, both page sizes, row tiles that
+    # leave rows unused, chunks spanning several key tiles and a ragged tail
+    (2, 16, 16, 128, 16, (300, 129), (300, 1), "bf16"),
+    (3, 32, 16, 128, 32, (1000, 517, 64), (200, 17, 64), "f16"),
+    (2, 64, 16, 128, 16, (777, 2048), (130, 33), "bf16"),
+    (1, 32, 2, 128, 32, (1500,), (100,), "bf16"),
+    (2, 24, 2, 128, 32, (400, 260), (260, 260), "f16"),
+    (2, 40, 8, 128, 16, (129, 3000), (129, 77), "f16"),
 ]
 
 
@@ -274,6 +282,51 @@ def test_prefill_row_independent_of_later_rows():
         pois["v_cache"][pg, j % 32] = inputs.round_to(np.array([-50.0]), "bf16")[0]
     got, _ = gpu_prefill(pois, meta)
     assert bitwise_equal(got[: r + 1], base[: r + 1])
+
+
+def test_prefill_poisoned_unread_memory_changes_nothing():
+    """Prefill twin of the decode poisoning test: NaN in unreferenced pages and
+    in the slots past each context in its last page never reach the output."""
+    inp, meta = problem(B=3, Hq=16, Hkv=4, D=128, P=32, lens=(45, 200, 97), qlens=(45, 20, 60),
+                        dt="bf16", num_pages=16, seed=43)
+    base, st0 = gpu_prefill(inp, meta)
+    pois = dict(inp, k_cache=inp["k_cache"].copy(), v_cache=inp["v_cache"].copy())
+    used = set(int(x) for x in inp["block_tables"].reshape(-1) if x >= 0)
+    nan = np.uint16(0x7FC0)  # bf16 quiet NaN (storage bits)
+    for pg in range(16):
+        if pg not in used:
+            pois["k_cache"][pg] = nan
+            pois["v_cache"][pg] = nan
+    for s, L in enumerate(inp["context_lens"]):
+        last = inp["block_tables"][s][(L - 1) // 32]
+        if L % 32:
+            pois["k_cache"][last, L % 32:] = nan
+            pois["v_cache"][last, L % 32:] = nan
+    got, status = gpu_prefill(pois, meta)
+    assert st0 == 0 and status == 0 and bitwise_equal(got, base)
+    assert_within(got, oracle.attention(inp, threads=THREADS, **meta), TOL["bf16"], "poisoned")
+
+
+def test_prefill_bad_page_flags_and_skips():
+    inp, meta = problem(B=2, Hq=16, Hkv=2, D=128, P=32, lens=(300, 300), qlens=(40, 40),
+                        dt="bf16", num_pages=20, seed=65)
+    bad = dict(inp, block_tables=inp["block_tables"].copy())
+    bad["block_tables"][1, 2] = 5000  # outside the pool
+    got, status = gpu_prefill(bad, meta)
+    assert status & ops.PA_DEV_BAD_PAGE
+    assert np.isfinite(got).all()
+    ref = oracle.attention(inp, threads=THREADS, **meta)
+    assert_within(got[:40], ref[:40], TOL["bf16"], "unaffected sequence")
+
+
+def test_prefill_bad_length_flags_and_zeroes():
+    inp, meta = problem(B=2, Hq=16, Hkv=2, D=128, P=32, lens=(64, 64), qlens=(32, 32),
+                        dt="bf16", num_pages=8, seed=67)
+    bad = dict(inp, context_lens=np.array([64, 10], dtype=np.int32))  # L < chunk rows
+    got, status = gpu_prefill(bad, meta)
+    assert status & ops.PA_DEV_BAD_LEN
+    assert np.array_equal(got[32:], np.zeros_like(got[32:]))
+    assert_within(got[:32], oracle.attention(inp, threads=THREADS, **meta)[:32], TOL["bf16"], "ok seq")
 
 
 # ---------------------------------------------------------- device errors --
