@@ -321,7 +321,7 @@ PA_EXPORT pa_status pa_prefill_chunk(const pa_params* p, const void* q, const in
     a.max_q_len = max_q_len;
     a.total_q = total_q;
     a.num_splits = 1;
-    if (pa::prefill_tc_supported(p->kv_dtype, p->head_dim, p->page_size, r.group))
+    if (pa::prefill_tc_supported(p->kv_dtype, p->head_dim, p->page_size, r.group, p->scale))
         return cuda_status(pa::launch_prefill_tc(a, p->kv_dtype, p->head_dim, p->page_size, stream));
     return cuda_status(pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
 }

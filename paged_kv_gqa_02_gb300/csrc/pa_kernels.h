@@ -32,8 +32,8 @@ struct DecodeV1Call {
     int phases;  // bit 0: partial kernel, bit 1: combine kernel
 };
 // Chunked prefill on the tensor cores (tcgen05): 16-bit Q/K/V, head_dim 128,
-// pages of 16 or 32 slots, G = Hq/Hkv <= 16.  Grid (Hkv * B, row tiles).
-bool prefill_tc_supported(pa_dtype dt, int D, int P, int G);
+// pages of 16 or 32 slots, G = Hq/Hkv <= 16, scale > 0.  Grid (Hkv * B, row tiles).
+bool prefill_tc_supported(pa_dtype dt, int D, int P, int G, float scale);
 cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st);
 
 size_t decode_v1_workspace_bytes(int B, int Hq, int Hkv, int D, int n_ctas);

@@ -11,19 +11,27 @@
 // Row r of a chunk of T rows over a context of L keys sees keys 0..L-T+r
 // (crucible README, "Prefill scheduling").
 //
-// Warp roles (192 threads):
-//   warp 0     TMA producer: Q once, then K/V tiles into a 3-stage ring
-//   warp 1     tensor-memory owner and MMA issuer (one thread)
-//   warps 2-5  softmax: one thread per MMA row (tensor-memory lane), online
-//              softmax in base 2 with a lazily raised running max, the
-//              probabilities written back to tensor memory as hi + lo
-//              16-bit parts, and the epilogue (O / l to global memory)
+// Each CTA owns two such row tiles, A and B (consecutive chunk rows), that
+// share every K/V tile: K/V reaches shared memory once per 256 query rows,
+// and the two softmax warpgroups take turns with the tensor cores.
 //
-// Tensor memory (512 columns): S double buffer [0,256), P hi [256,320),
-// P lo [320,384), O [384,512).  Per key tile j the MMA thread issues
-// S_j = Q K_j^T (both operands K-major from shared memory), then, once the
-// softmax has written P_{j-1}, O += P_{j-1} V_{j-1} (P from tensor memory,
-// V MN-major from shared memory).
+// Warp roles (320 threads):
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one thread
+//              per MMA row (tensor-memory lane), online softmax in base 2
+//              with a lazily raised running max, probabilities written back
+//              over their scores as hi + lo 16-bit parts, and the epilogue
+//              (O / l to global memory)
+//   warp 8     TMA producer: Q once, then K and V tiles into their rings
+//              (one lane per page issues that page's boxes)
+//   warp 9     tensor-memory owner and MMA issuer (one thread)
+//
+// Tensor memory (512 columns): S/P of tile A [0,128), S/P of tile B
+// [128,256), O of A [256,384), O of B [384,512).  Per key tile j the MMA
+// thread issues P_A(j).V_j, then S_A(j+1) = Q_A K_{j+1}^T once that P.V has
+// finished reading P_A (same columns), then P_B(j).V_j and S_B(j+1): while
+// one warpgroup computes its softmax, the tensor cores work for the other.
+// Both operands of Q K^T are K-major in shared memory; P is read from
+// tensor memory and V is MN-major in shared memory.
 //
 // Probabilities are split as p = hi + lo with both parts in the K/V type
 // and both multiplied by V (two MMAs per 16 keys), so P carries ~16
@@ -42,26 +50,28 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;          // head_dim served by this kernel
-constexpr int kBM = 128;         // MMA rows
+constexpr int kBM = 128;         // MMA rows per row tile
 constexpr int kBN = 128;         // keys per tile
-constexpr int kStages = 3;       // K/V ring depth
-constexpr int kThreads = 192;
-constexpr uint32_t kTileBytes = kBN * kD * 2;  // one K (or V) tile
+constexpr int kKS = 3;           // K ring depth
+constexpr int kVS = 2;           // V ring depth
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTileBytes = kBN * kD * 2;  // one K (or V, or Q) tile
 constexpr uint32_t kHalfBytes = kBN * 128;     // one 64-dim half of a tile
-constexpr uint32_t kStageBytes = 2 * kTileBytes;
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kStageOff = kQOff + kBM * kD * 2;
-constexpr uint32_t kBarOff = kStageOff + kStages * kStageBytes;
-constexpr uint32_t kNumBars = 18;  // 17 in use, rounded to keep the slot 16-byte aligned
+constexpr uint32_t kQOff = 0;                  // Q of A, then Q of B
+constexpr uint32_t kKOff = kQOff + 2 * kTileBytes;
+constexpr uint32_t kVOff = kKOff + kKS * kTileBytes;
+constexpr uint32_t kBarOff = kVOff + kVS * kTileBytes;
+constexpr uint32_t kNumBars = 1 + 2 * kKS + 2 * kVS + 2 * 3 + 1;
 constexpr uint32_t kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kRescaleStep = 8.f;  // raise the running max only when it grows by > 2^8
+constexpr uint32_t kNegInf = 0xff800000u;
 
-// tensor-memory columns
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColPhi = 256;
-constexpr uint32_t kColPlo = 320;
-constexpr uint32_t kColO = 384;
+// tensor-memory columns of tile x (0 = A, 1 = B)
+__device__ inline uint32_t col_s(int x) { return 128u * x; }
+__device__ inline uint32_t col_o(int x) { return 256u + 128u * x; }
 
 struct TcParams {
     const int32_t* cu_q_lens;
@@ -71,7 +81,7 @@ struct TcParams {
     uint32_t* dev_status;
     int32_t Hq, Hkv, G, tq, P, num_pages, max_blocks, max_q_len, total_q;
     int32_t head_first;
-    float scale_log2;
+    float scale_log2;  // > 0
 };
 
 // Bounded wait that also gives up when another role has aborted.
@@ -88,14 +98,22 @@ __device__ inline void raise_abort(volatile uint32_t* abort_flag, uint32_t* dev_
     flag(dev_status, PA_DEV_TIMEOUT);
 }
 
+__device__ inline float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // hi/lo split of two probabilities into packed 16-bit pairs (low half = even key)
 template <typename T> struct Pack;
 template <> struct Pack<__nv_bfloat16> {
+    // hi keeps the top 16 bits (truncation); lo = p - hi is exact in fp32 and
+    // rounded to bf16, so hi + lo carries ~16 significant bits
     __device__ static inline void split(float a, float b, uint32_t& hi, uint32_t& lo) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        const float2 hf = __bfloat1622float2(h);
-        const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-        hi = *reinterpret_cast<const uint32_t*>(&h);
+        const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+        hi = __byte_perm(ua, ub, 0x7632);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(a - __uint_as_float(ua & 0xffff0000u),
+                                                       b - __uint_as_float(ub & 0xffff0000u));
         lo = *reinterpret_cast<const uint32_t*>(&l);
     }
 };
@@ -109,29 +127,52 @@ template <> struct Pack<__half> {
     }
 };
 
+// Visible keys of one 32-key chunk as a bit mask: the first `nvis` keys,
+// minus those in pages outside the pool.
+__device__ inline uint32_t chunk_mask(int nvis, uint32_t pmask, int c, int P) {
+    uint32_t m = nvis >= 32 ? 0xffffffffu : (nvis <= 0 ? 0u : ((1u << nvis) - 1u));
+    if (P == 32) {
+        if (!((pmask >> c) & 1u)) m = 0u;
+    } else {  // 16-slot pages: two per chunk
+        m &= (((pmask >> (2 * c)) & 1u) ? 0x0000ffffu : 0u) | (((pmask >> (2 * c + 1)) & 1u) ? 0xffff0000u : 0u);
+    }
+    return m;
+}
+
+__device__ inline void apply_mask(uint32_t (&r)[32], uint32_t m) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) r[k] = ((m >> k) & 1u) ? r[k] : kNegInf;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const TcParams a) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     const int g = blockIdx.x % a.Hkv, b = blockIdx.x / a.Hkv;
-    const int tile = gridDim.y - 1 - blockIdx.y;  // heaviest row tiles first
+    const int pair = gridDim.y - 1 - blockIdx.y;  // heaviest row tiles first
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = a.G, P = a.P;
+    const int G = a.G, P = a.P, tq = a.tq;
 
-    // ---- rows of this tile and their causal ends --------------------------------
+    // ---- rows of the two tiles and their causal ends ----------------------------
     const int L = a.context_lens[b];
     const int row0 = a.cu_q_lens[b];
     const int Tq = a.cu_q_lens[b + 1] - row0;
     const bool bad = Tq < 0 || row0 < 0 || L < Tq || L > a.max_blocks * P || Tq > a.max_q_len;
-    const int r_first = tile * a.tq;
+    const int r_first = pair * 2 * tq;  // first chunk row of tile A
     const int t_rows = max(0, min(Tq, a.max_q_len));
-    const int n_rows =
-        row0 < 0 ? 0 : max(0, min(min(a.tq, t_rows - r_first), a.total_q - (row0 + r_first)));
-    if (bad && tile == 0 && tid == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
-    if (n_rows <= 0) return;
-    if (bad) {  // no key is read; the tile's rows are written as zeros
-        for (int i = tid; i < n_rows * G * (kD / 4); i += kThreads) {
+    // rows of tile x that exist: below T (and the host bound), inside q/out
+    auto rows_of = [&](int x) {
+        const int r = r_first + x * tq;
+        return row0 < 0 ? 0 : max(0, min(min(tq, t_rows - r), a.total_q - (row0 + r)));
+    };
+    const int n_rows_a = rows_of(0), n_rows_b = rows_of(1);
+    const bool has_b = n_rows_b > 0;
+    if (bad && pair == 0 && tid == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
+    if (n_rows_a <= 0) return;
+    if (bad) {  // no key is read; the rows are written as zeros
+        const int n = (n_rows_a + n_rows_b) * G * (kD / 4);
+        for (int i = tid; i < n; i += kThreads) {
             const int r = i / (G * (kD / 4)), rest = i % (G * (kD / 4));
             const int h = rest / (kD / 4), c = rest % (kD / 4);
             float* o = a.out + (int64_t(row0 + r_first + r) * a.Hq + g * G + h) * kD;
@@ -140,10 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     const int start = L - Tq;
-    const int kend = start + r_first + n_rows;  // keys [0, kend) are visible to some row
+    // keys [0, kend) are visible to some row of the CTA
+    const int kend = start + r_first + (has_b ? tq + n_rows_b : n_rows_a);
     const int nt = (kend + kBN - 1) / kBN;
-    const int npg = (kend + P - 1) / P;         // pages holding visible keys
-    const int PT = kBN / P;                     // pages per key tile
+    const int npg = (kend + P - 1) / P;  // pages holding visible keys
+    const int PT = kBN / P;              // pages per key tile
     const int32_t* table = a.block_tables + int64_t(b) * a.max_blocks;
 
     // ---- shared memory ------------------------------------------------------------
@@ -153,37 +195,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sQ = base + kQOff;
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOff);
     uint64_t* q_full = bars;
-    uint64_t* k_full = bars + 1;
-    uint64_t* v_full = bars + 1 + kStages;
-    uint64_t* kv_empty = bars + 1 + 2 * kStages;
-    uint64_t* s_full = bars + 1 + 3 * kStages;
-    uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_free + 2;
-    uint64_t* o_done = p_full + 1;
-    uint64_t* mma_done = o_done + 1;
+    uint64_t* k_full = q_full + 1;
+    uint64_t* k_empty = k_full + kKS;
+    uint64_t* v_full = k_empty + kKS;
+    uint64_t* v_empty = v_full + kVS;
+    uint64_t* s_full = v_empty + kVS;  // [2]: S of tile x complete
+    uint64_t* p_full = s_full + 2;     // [2]: P of tile x written (4 softmax warps)
+    uint64_t* o_done = p_full + 2;     // [2]: one phase per P.V of tile x
+    uint64_t* mma_done = o_done + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars);
     volatile uint32_t* abort_flag = tslot + 1;
-    auto stage_k = [&](int st) { return base + kStageOff + st * kStageBytes; };
-    auto stage_v = [&](int st) { return base + kStageOff + st * kStageBytes + kTileBytes; };
+    auto k_tile = [&](int st) { return base + kKOff + st * kTileBytes; };
+    auto v_tile = [&](int st) { return base + kVOff + st * kTileBytes; };
 
     if (tid == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kKS; ++i) {
             mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < kVS; ++i) {
             mbar_init(&v_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0u;
         mbar_fence_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
@@ -192,127 +236,143 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tm = *tslot;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ================================ producer ================================
+        const int xc = a.head_first ? g : 0, yc = a.head_first ? 0 : g;
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             // full box bytes count even where the box leaves the tensor (zero fill)
-            mbar_arrive_expect_tx(q_full, 2u * 128u * uint32_t(G * a.tq));
-            tma_load_3d(sQ, &tmQ, q_full, 0, g * G, row0 + r_first);
-            tma_load_3d(sQ + kHalfBytes, &tmQ, q_full, 64, g * G, row0 + r_first);
-            const int xc = a.head_first ? g : 0, yc = a.head_first ? 0 : g;
-            int issued = 0;
-            for (int j = 0; j < nt; ++j) {
-                const int st = j % kStages;
-                if (j >= kStages && !wait_bar(&kv_empty[st], ((j / kStages) - 1) & 1, abort_flag)) {
-                    raise_abort(abort_flag, a.dev_status);
-                    break;
-                }
-                int pg[8];
+            const uint32_t qbytes = 2u * 128u * uint32_t(G * tq);
+            mbar_arrive_expect_tx(q_full, has_b ? 2 * qbytes : qbytes);
+            for (int x = 0; x < (has_b ? 2 : 1); ++x)
+                for (int hh = 0; hh < 2; ++hh)
+                    tma_load_3d(sQ + x * kTileBytes + hh * kHalfBytes, &tmQ, q_full, 64 * hh, g * G,
+                                row0 + r_first + x * tq);
+        }
+        // lane p issues both halves of page p of each tile
+        auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int pg) {
+            if (lane == 0) mbar_arrive_expect_tx(bar, kTileBytes);
+            __syncwarp();
+            if (lane < PT)
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    const int idx = j * PT + p;
-                    pg[p] = a.num_pages;  // beyond the tensor: the box reads as zeros
-                    if (p < PT && idx < npg) {
-                        const int e = table[idx];
-                        if (e >= 0 && e < a.num_pages)
-                            pg[p] = e;
-                        else
-                            flag(a.dev_status, PA_DEV_BAD_PAGE);
-                    }
-                }
-                uint8_t* sK = stage_k(st);
-                uint8_t* sV = stage_v(st);
-                mbar_arrive_expect_tx(&k_full[st], kTileBytes);
-#pragma unroll
-                for (int p = 0; p < 8; ++p)
-                    if (p < PT)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh)
-                            tma_load_4d(sK + hh * kHalfBytes + p * P * 128, &tmK, &k_full[st], 64 * hh, xc,
-                                        yc, pg[p]);
-                mbar_arrive_expect_tx(&v_full[st], kTileBytes);
-#pragma unroll
-                for (int p = 0; p < 8; ++p)
-                    if (p < PT)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh)
-                            tma_load_4d(sV + hh * kHalfBytes + p * P * 128, &tmV, &v_full[st], 64 * hh, xc,
-                                        yc, pg[p]);
-                issued = j + 1;
+                for (int hh = 0; hh < 2; ++hh)
+                    tma_load_4d(dst + hh * kHalfBytes + lane * P * 128, map, bar, 64 * hh, xc, yc, pg);
+        };
+        int kq = 0, vq = 0;  // tiles issued
+        bool ok = true;
+        for (int j = 0; ok && j < nt; ++j) {
+            // physical page of lane's slot in tile j (out-of-pool entries flagged, read as zeros)
+            int pg = a.num_pages;  // beyond the tensor: the box reads as zeros
+            const int idx = j * PT + lane;
+            if (lane < PT && idx < npg) {
+                const int e = table[idx];
+                if (e >= 0 && e < a.num_pages)
+                    pg = e;
+                else
+                    flag(a.dev_status, PA_DEV_BAD_PAGE);
             }
+            const int sk = j % kKS, sv = j % kVS;
+            if (j >= kKS) ok = __all_sync(0xffffffffu, wait_bar(&k_empty[sk], ((j / kKS) - 1) & 1, abort_flag));
+            if (!ok) break;
+            load_tile(k_tile(sk), &tmK, &k_full[sk], pg);
+            kq = j + 1;
+            if (j >= kVS) ok = __all_sync(0xffffffffu, wait_bar(&v_empty[sv], ((j / kVS) - 1) & 1, abort_flag));
+            if (!ok) break;
+            load_tile(v_tile(sv), &tmV, &v_full[sv], pg);
+            vq = j + 1;
+        }
+        if (lane == 0) {
+            if (!ok) raise_abort(abort_flag, a.dev_status);
             // never leave the CTA with copies in flight
-            for (int j = max(0, issued - kStages); j < issued; ++j) {
-                const int st = j % kStages;
-                mbar_wait(&k_full[st], (j / kStages) & 1, kWaitLimit);
-                mbar_wait(&v_full[st], (j / kStages) & 1, kWaitLimit);
-            }
+            for (int j = max(0, kq - kKS); j < kq; ++j) mbar_wait(&k_full[j % kKS], (j / kKS) & 1, kWaitLimit);
+            for (int j = max(0, vq - kVS); j < vq; ++j) mbar_wait(&v_full[j % kVS], (j / kVS) & 1, kWaitLimit);
             if (!mbar_wait(q_full, 0, kWaitLimit)) flag(a.dev_status, PA_DEV_TIMEOUT);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ================================== MMA ===================================
         if (lane == 0) {
             const uint32_t idQK = tc::idesc_f16(kBM, kBN, kBf16, false);
             const uint32_t idPV = tc::idesc_f16(kBM, kD, kBf16, true);
-            const uint32_t q_addr = smem_u32(sQ);
+            const int nx = has_b ? 2 : 1;
             bool ok = wait_bar(q_full, 0, abort_flag);
             tc::fence_after_sync();
-            auto pv = [&](int i) -> bool {
-                const int st = i % kStages;
-                if (!wait_bar(p_full, i & 1, abort_flag)) return false;
-                if (!wait_bar(&v_full[st], (i / kStages) & 1, abort_flag)) return false;
-                tc::fence_after_sync();
-                const uint32_t v_addr = smem_u32(stage_v(st));
-#pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks) {
-                    // 16 keys: 8-row core groups 1024 B apart, dim halves 16 KB apart
-                    const uint64_t bd = tc::smem_desc_sw128(v_addr + ks * 2048, kHalfBytes, 1024);
-                    tc::mma_ts(tm + kColO, tm + kColPhi + ks * 8, bd, idPV, i > 0 || ks > 0);
-                    tc::mma_ts(tm + kColO, tm + kColPlo + ks * 8, bd, idPV, true);
-                }
-                tc::commit(&kv_empty[st]);
-                tc::commit(o_done);
-                return true;
-            };
-            for (int j = 0; ok && j < nt; ++j) {
-                const int st = j % kStages, sb = j & 1;
-                ok = wait_bar(&k_full[st], (j / kStages) & 1, abort_flag);
-                if (ok && j >= 2) ok = wait_bar(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
-                if (!ok) break;
-                tc::fence_after_sync();
-                const uint32_t k_addr = smem_u32(stage_k(st));
+            // S_x = Q_x K_j^T into the columns of tile x
+            auto qk = [&](int x, int j) {
+                const uint32_t q_addr = smem_u32(sQ + x * kTileBytes);
+                const uint32_t k_addr = smem_u32(k_tile(j % kKS));
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-                    tc::mma_ss(tm + kColS + sb * kBN, tc::smem_desc_sw128(q_addr + off, 16, 1024),
+                    tc::mma_ss(tm + col_s(x), tc::smem_desc_sw128(q_addr + off, 16, 1024),
                                tc::smem_desc_sw128(k_addr + off, 16, 1024), idQK, ks > 0);
                 }
-                tc::commit(&s_full[sb]);
-                if (j >= 1) ok = pv(j - 1);
+                tc::commit(&s_full[x]);
+            };
+            // O_x += P_x V_j, P_x read from the score columns of tile x
+            auto pv = [&](int x, int j) {
+                const uint32_t v_addr = smem_u32(v_tile(j % kVS));
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks) {
+                    // 16 keys: 8-row core groups 1024 B apart, dim halves 16 KB apart.
+                    // P of keys 32c..32c+31 sits in columns 32c (hi, 16) and 32c+16 (lo, 16).
+                    const uint64_t bd = tc::smem_desc_sw128(v_addr + ks * 2048, kHalfBytes, 1024);
+                    const uint32_t col = col_s(x) + 32 * (ks >> 1) + 8 * (ks & 1);
+                    tc::mma_ts(tm + col_o(x), tm + col, bd, idPV, j > 0 || ks > 0);
+                    tc::mma_ts(tm + col_o(x), tm + col + 16, bd, idPV, true);
+                }
+                tc::commit(&o_done[x]);
+            };
+            if (ok) ok = wait_bar(&k_full[0], 0, abort_flag);
+            if (ok) {
+                tc::fence_after_sync();
+                for (int x = 0; x < nx; ++x) qk(x, 0);
+                tc::commit(&k_empty[0]);
             }
-            if (ok) ok = pv(nt - 1);
+            for (int j = 0; ok && j < nt; ++j) {
+                for (int x = 0; ok && x < nx; ++x) {
+                    ok = wait_bar(&p_full[x], j & 1, abort_flag);
+                    if (ok && x == 0) ok = wait_bar(&v_full[j % kVS], (j / kVS) & 1, abort_flag);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    pv(x, j);
+                    if (x == nx - 1) tc::commit(&v_empty[j % kVS]);
+                    if (j + 1 < nt) {
+                        // the next S of tile x overwrites P_x: wait until P_x.V is done
+                        if (x == 0) ok = wait_bar(&k_full[(j + 1) % kKS], ((j + 1) / kKS) & 1, abort_flag);
+                        if (ok) ok = wait_bar(&o_done[x], j & 1, abort_flag);
+                        if (!ok) break;
+                        tc::fence_after_sync();
+                        qk(x, j + 1);
+                        if (x == nx - 1) tc::commit(&k_empty[(j + 1) % kKS]);
+                    }
+                }
+            }
             if (!ok) raise_abort(abort_flag, a.dev_status);
             // every MMA issued so far has finished before tensor memory is freed
             tc::commit(mma_done);
             if (!mbar_wait(mma_done, 0, kWaitLimit)) flag(a.dev_status, PA_DEV_TIMEOUT);
         }
-    } else {
+    } else if (warp < 4 || has_b) {
         // ================================= softmax =================================
+        const int x = warp >> 2;  // tile
         const int quad = warp & 3;
         const int m = quad * 32 + lane;  // MMA row = tensor-memory lane
         const uint32_t lane_addr = uint32_t(quad * 32) << 16;
         const int t = m / G, h = m - (m / G) * G;
-        const bool row_ok = t < a.tq && t < n_rows;
-        const int lim = row_ok ? start + r_first + t + 1 : 0;  // keys [0, lim)
+        const int n_rows = x ? n_rows_b : n_rows_a;
+        const int r_tile = r_first + x * tq;
+        const bool row_ok = t < tq && t < n_rows;
+        const int lim = row_ok ? start + r_tile + t + 1 : 0;  // keys [0, lim)
         const float sl2 = a.scale_log2;
-        const int pshift = P == 16 ? 4 : 5;
+        const uint32_t sbase = tm + lane_addr + col_s(x);
+        const uint32_t obase = tm + lane_addr + col_o(x);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        uint32_t s[4][32];
+        uint32_t ra[32], rb[32];
         for (int j = 0; j < nt; ++j) {
-            const int sb = j & 1, st = j % kStages, k0 = j * kBN;
+            const int k0 = j * kBN;
             // pages of this tile outside the pool are skipped (flagged by the producer)
             bool pok = true;
             {
@@ -322,89 +382,106 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pok = e >= 0 && e < a.num_pages;
                 }
             }
-            ok = __all_sync(0xffffffffu, wait_bar(&s_full[sb], (j >> 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, wait_bar(&s_full[x], j & 1, abort_flag));
             if (!ok) break;
             tc::fence_after_sync();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tc::ld_32x32b_x32(tm + lane_addr + kColS + sb * kBN + 32 * c, s[c]);
-            tc::wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[sb]);
             const uint32_t pmask = __ballot_sync(0xffffffffu, pok);
+            const bool full = (k0 + kBN <= lim) && pmask == 0xffffffffu;
 
-            // scores in base-2 units, masked keys at -inf
+            // ---- pass 1: row max of the raw scores (scale > 0 keeps the order)
             float mx = -INFINITY;
-            if (k0 + kBN <= lim && pmask == 0xffffffffu) {
+            tc::ld_32x32b_x32(sbase, ra);
+            tc::ld_32x32b_x32(sbase + 32, rb);
+            tc::wait_ld();
+            tc::reg_fence(ra);
+            tc::reg_fence(rb);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; c += 2) {
+                if (!full) {
+                    apply_mask(ra, chunk_mask(lim - k0 - 32 * c, pmask, c, P));
+                    apply_mask(rb, chunk_mask(lim - k0 - 32 * (c + 1), pmask, c + 1, P));
+                }
+                float m0 = mx, m1 = -INFINITY;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float x = __uint_as_float(s[c][k]) * sl2;
-                        s[c][k] = __float_as_uint(x);
-                        mx = fmaxf(mx, x);
-                    }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int key = k0 + 32 * c + k;
-                        const bool vis = key < lim && ((pmask >> ((32 * c + k) >> pshift)) & 1u);
-                        const float x = vis ? __uint_as_float(s[c][k]) * sl2 : -INFINITY;
-                        s[c][k] = __float_as_uint(x);
-                        mx = fmaxf(mx, x);
-                    }
+                for (int k = 0; k < 32; k += 4) {
+                    m0 = max3(m0, __uint_as_float(ra[k]), __uint_as_float(ra[k + 1]));
+                    m1 = max3(m1, __uint_as_float(ra[k + 2]), __uint_as_float(ra[k + 3]));
+                    m0 = max3(m0, __uint_as_float(rb[k]), __uint_as_float(rb[k + 1]));
+                    m1 = max3(m1, __uint_as_float(rb[k + 2]), __uint_as_float(rb[k + 3]));
+                }
+                mx = fmaxf(m0, m1);
+                if (c == 0) {
+                    tc::ld_32x32b_x32(sbase + 64, ra);
+                    tc::ld_32x32b_x32(sbase + 96, rb);
+                    tc::wait_ld();
+                    tc::reg_fence(ra);
+                    tc::reg_fence(rb);
+                }
             }
-            const bool need = mx > m_run + kRescaleStep;
-            const float alpha = need ? ex2(m_run - mx) : 1.f;
-            if (need) m_run = mx;
+            const float mt = mx * sl2;  // -inf when nothing is visible
+            const bool need = mt > m_run + kRescaleStep;
+            const float alpha = need ? ex2(m_run - mt) : 1.f;
+            if (need) m_run = mt;
             l_run *= alpha;
 
-            // O and the P buffer are free once PV_{j-1} has finished
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, wait_bar(o_done, (j - 1) & 1, abort_flag));
-                if (!ok) break;
-                tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, need)) {
-                    uint32_t o[32];
+            // O_x is rescaled in place: P_x(j-1).V has finished (S_x(j) was
+            // issued after it)
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                    for (int c = 0; c < kD / 32; ++c) {
-                        tc::ld_32x32b_x32(tm + lane_addr + kColO + 32 * c, o);
-                        tc::wait_ld();
+                for (int c = 0; c < kD / 32; ++c) {
+                    tc::ld_32x32b_x32(obase + 32 * c, ra);
+                    tc::wait_ld();
+                    tc::reg_fence(ra);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tc::st_32x32b_x32(tm + lane_addr + kColO + 32 * c, o);
-                    }
+                    for (int k = 0; k < 32; ++k) ra[k] = __float_as_uint(__uint_as_float(ra[k]) * alpha);
+                    tc::st_32x32b_x32(obase + 32 * c, ra);
                 }
             }
 
-            // probabilities: p = 2^(x - m_run), split hi + lo, into tensor memory
-            const float mu = m_run == -INFINITY ? 0.f : m_run;
-            float sum = 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {  // keys 32c .. 32c+31 -> columns 16c .. 16c+15
+            // ---- pass 2: p = 2^(s * scale_log2 - m_run), split hi + lo, written
+            // over the scores: keys 32c.. -> columns 32c (hi) and 32c + 16 (lo)
+            const float nmu = m_run == -INFINITY ? 0.f : -m_run;
+            float sum0 = 0.f, sum1 = 0.f;
+            auto emit = [&](uint32_t (&r)[32], int c) {
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int w = 0; w < 16; ++w) {
-                    const float p0 = ex2(__uint_as_float(s[c][2 * w]) - mu);
-                    const float p1 = ex2(__uint_as_float(s[c][2 * w + 1]) - mu);
-                    sum += p0 + p1;
+                    const float p0 = ex2(fmaf(__uint_as_float(r[2 * w]), sl2, nmu));
+                    const float p1 = ex2(fmaf(__uint_as_float(r[2 * w + 1]), sl2, nmu));
+                    sum0 += p0;
+                    sum1 += p1;
                     Pack<T>::split(p0, p1, hi[w], lo[w]);
                 }
-                tc::st_32x32b_x16(tm + lane_addr + kColPhi + 16 * c, hi);
-                tc::st_32x32b_x16(tm + lane_addr + kColPlo + 16 * c, lo);
+                tc::st_32x32b_x16(sbase + 32 * c, hi);
+                tc::st_32x32b_x16(sbase + 32 * c + 16, lo);
+            };
+            tc::ld_32x32b_x32(sbase, ra);
+            tc::wait_ld();
+            tc::reg_fence(ra);
+#pragma unroll 1
+            for (int c = 0; c < 4; c += 2) {
+                tc::ld_32x32b_x32(sbase + 32 * (c + 1), rb);
+                if (!full) apply_mask(ra, chunk_mask(lim - k0 - 32 * c, pmask, c, P));
+                emit(ra, c);
+                tc::wait_ld();
+                tc::reg_fence(rb);
+                if (c + 2 < 4) tc::ld_32x32b_x32(sbase + 32 * (c + 2), ra);
+                if (!full) apply_mask(rb, chunk_mask(lim - k0 - 32 * (c + 1), pmask, c + 1, P));
+                emit(rb, c + 1);
+                tc::wait_ld();
+                tc::reg_fence(ra);
             }
-            l_run += sum;
+            l_run += sum0 + sum1;
             tc::wait_st();
 
             // slots past the context in its last page may hold anything (NaN):
-            // zero those V rows so that 0 * V stays 0
+            // tile A's warps zero those V rows (before either P.V reads them)
             const int zlo = L - k0, zhi = min(kBN, npg * P - k0);
-            if (zlo < zhi) {
-                ok = __all_sync(0xffffffffu, wait_bar(&v_full[st], (j / kStages) & 1, abort_flag));
+            if (x == 0 && zlo < zhi) {
+                const int sv = j % kVS;
+                ok = __all_sync(0xffffffffu, wait_bar(&v_full[sv], (j / kVS) & 1, abort_flag));
                 if (!ok) break;
-                uint8_t* sV = stage_v(st);
+                uint8_t* sV = v_tile(sv);
                 for (int i = m; i < (zhi - zlo) * 16; i += kBM) {
                     const int row = zlo + (i >> 4), c = i & 15;
                     *reinterpret_cast<uint4*>(sV + (c >> 3) * kHalfBytes + row * 128 + (c & 7) * 16) =
@@ -414,27 +491,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[x]);
         }
 
         // ---- epilogue: O / l ------------------------------------------------------
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar(o_done, (nt - 1) & 1, abort_flag));
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&o_done[x], (nt - 1) & 1, abort_flag));
         if (ok) {
             tc::fence_after_sync();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            float* orow = a.out + (int64_t(row0 + r_first + t) * a.Hq + g * G + h) * kD;
-            uint32_t o[32];
+            float* orow = a.out + (int64_t(row0 + r_tile + t) * a.Hq + g * G + h) * kD;
 #pragma unroll 1
             for (int c = 0; c < kD / 32; ++c) {
-                tc::ld_32x32b_x32(tm + lane_addr + kColO + 32 * c, o);
+                tc::ld_32x32b_x32(obase + 32 * c, ra);
                 tc::wait_ld();
+                tc::reg_fence(ra);
                 if (row_ok) {
                     float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                             __uint_as_float(o[4 * k + 2]) * inv,
-                                             __uint_as_float(o[4 * k + 3]) * inv);
+                        dst[k] = make_float4(__uint_as_float(ra[4 * k]) * inv, __uint_as_float(ra[4 * k + 1]) * inv,
+                                             __uint_as_float(ra[4 * k + 2]) * inv,
+                                             __uint_as_float(ra[4 * k + 3]) * inv);
                 }
             }
         } else {
@@ -444,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tm, 512);
     }
@@ -479,12 +556,12 @@ cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 
 }  // namespace
 
-bool prefill_tc_supported(pa_dtype dt, int D, int P, int G) {
-    return dt != PA_F32 && D == kD && (P == 16 || P == 32) && G >= 1 && G <= kMaxGroup;
+bool prefill_tc_supported(pa_dtype dt, int D, int P, int G, float scale) {
+    return dt != PA_F32 && D == kD && (P == 16 || P == 32) && G >= 1 && G <= kMaxGroup && scale > 0.f;
 }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st) {
-    if (!prefill_tc_supported(dt, D, P, a.group)) return cudaErrorInvalidValue;
+    if (!prefill_tc_supported(dt, D, P, a.group, a.scale_log2)) return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int G = a.group;
@@ -551,7 +628,7 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cuda
     p.total_q = a.total_q;
     p.head_first = head_first;
     p.scale_log2 = a.scale_log2;
-    const int n_tiles = (a.max_q_len + tq - 1) / tq;
+    const int n_tiles = (a.max_q_len + 2 * tq - 1) / (2 * tq);  // pairs of row tiles
     if (n_tiles > 65535 || int64_t(a.num_kv_heads) * a.num_seqs > 0x7fffffff) return cudaErrorInvalidValue;
     return dt == PA_BF16 ? launch_typed<__nv_bfloat16>(mq, mk, mv, p, n_tiles, a.num_seqs, st)
                          : launch_typed<__half>(mq, mk, mv, p, n_tiles, a.num_seqs, st);

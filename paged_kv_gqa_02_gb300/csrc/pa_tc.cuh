@@ -121,6 +121,15 @@ __device__ inline void st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
 __device__ inline void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ inline void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Registers written by tcgen05.ld are only valid after tcgen05.wait::ld.
+// The compiler sees the load's outputs as defined at the load, so each use
+// is tied to the wait through an empty asm that "rewrites" the registers.
+template <int N>
+__device__ inline void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // Tensor-memory address of (lane, column).
 __device__ inline uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) {
     return base + (lane << 16) + col;
