@@ -65,7 +65,9 @@ constexpr uint32_t kVOff = kKOff + kKS * kTileBytes;
 constexpr uint32_t kBarOff = kVOff + kVS * kTileBytes;
 constexpr uint32_t kNumBars = 1 + 2 * kKS + 2 * kVS + 2 * 3 + 1;
 constexpr uint32_t kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitLimit = 1u << 22;     // polls, for the final drains
+constexpr uint64_t kWaitNs = 2000000000ull;     // a role gives up after 2 s on one barrier
+constexpr uint32_t kSleepNs = 20000;            // longest sleep inside one try_wait
 constexpr float kRescaleStep = 8.f;  // raise the running max only when it grows by > 2^8
 constexpr uint32_t kNegInf = 0xff800000u;
 
@@ -84,13 +86,15 @@ struct TcParams {
     float scale_log2;  // > 0
 };
 
-// Bounded wait that also gives up when another role has aborted.
+// Bounded wait (by the global timer) that also gives up when another role
+// has aborted.  Waiting threads sleep inside try_wait rather than spin.
 __device__ inline bool wait_bar(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && *abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+        if (*abort_flag || globaltimer_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 
 __device__ inline void raise_abort(volatile uint32_t* abort_flag, uint32_t* dev_status) {
@@ -298,29 +302,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nx = has_b ? 2 : 1;
             bool ok = wait_bar(q_full, 0, abort_flag);
             tc::fence_after_sync();
+            // descriptors: the high word is shared, low words advance by offset >> 4
+            const uint32_t hi_d = tc::desc_hi_sw128(1024);
+            const uint32_t q_lo = tc::desc_lo(smem_u32(sQ), 16);
+            const uint32_t k_lo = tc::desc_lo(smem_u32(k_tile(0)), 16);
+            const uint32_t v_lo = tc::desc_lo(smem_u32(v_tile(0)), kHalfBytes);
             // S_x = Q_x K_j^T into the columns of tile x
             auto qk = [&](int x, int j) {
-                const uint32_t q_addr = smem_u32(sQ + x * kTileBytes);
-                const uint32_t k_addr = smem_u32(k_tile(j % kKS));
+                const uint32_t qx = q_lo + x * (kTileBytes >> 4);
+                const uint32_t kx = k_lo + (j % kKS) * (kTileBytes >> 4);
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-                    tc::mma_ss(tm + col_s(x), tc::smem_desc_sw128(q_addr + off, 16, 1024),
-                               tc::smem_desc_sw128(k_addr + off, 16, 1024), idQK, ks > 0);
+                    const uint32_t off = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+                    tc::mma_ss(tm + col_s(x), tc::make_desc(qx + off, hi_d), tc::make_desc(kx + off, hi_d), idQK,
+                               ks > 0);
                 }
                 tc::commit(&s_full[x]);
             };
             // O_x += P_x V_j, P_x read from the score columns of tile x
             auto pv = [&](int x, int j) {
-                const uint32_t v_addr = smem_u32(v_tile(j % kVS));
+                const uint32_t vx = v_lo + (j % kVS) * (kTileBytes >> 4);
+                const uint32_t p_col = tm + col_s(x), o_col = tm + col_o(x);
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks) {
                     // 16 keys: 8-row core groups 1024 B apart, dim halves 16 KB apart.
                     // P of keys 32c..32c+31 sits in columns 32c (hi, 16) and 32c+16 (lo, 16).
-                    const uint64_t bd = tc::smem_desc_sw128(v_addr + ks * 2048, kHalfBytes, 1024);
-                    const uint32_t col = col_s(x) + 32 * (ks >> 1) + 8 * (ks & 1);
-                    tc::mma_ts(tm + col_o(x), tm + col, bd, idPV, j > 0 || ks > 0);
-                    tc::mma_ts(tm + col_o(x), tm + col + 16, bd, idPV, true);
+                    const uint64_t bd = tc::make_desc(vx + ks * (2048 >> 4), hi_d);
+                    const uint32_t col = p_col + 32 * (ks >> 1) + 8 * (ks & 1);
+                    tc::mma_ts(o_col, col, bd, idPV, j > 0 || ks > 0);
+                    tc::mma_ts(o_col, col + 16, bd, idPV, true);
                 }
                 tc::commit(&o_done[x]);
             };
@@ -330,6 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int x = 0; x < nx; ++x) qk(x, 0);
                 tc::commit(&k_empty[0]);
             }
+            // per key tile and row tile x: P_x.V, then the next S_x, which
+            // overwrites P_x and so waits for that P.V to finish
             for (int j = 0; ok && j < nt; ++j) {
                 for (int x = 0; ok && x < nx; ++x) {
                     ok = wait_bar(&p_full[x], j & 1, abort_flag);
@@ -339,7 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pv(x, j);
                     if (x == nx - 1) tc::commit(&v_empty[j % kVS]);
                     if (j + 1 < nt) {
-                        // the next S of tile x overwrites P_x: wait until P_x.V is done
                         if (x == 0) ok = wait_bar(&k_full[(j + 1) % kKS], ((j + 1) / kKS) & 1, abort_flag);
                         if (ok) ok = wait_bar(&o_done[x], j & 1, abort_flag);
                         if (!ok) break;

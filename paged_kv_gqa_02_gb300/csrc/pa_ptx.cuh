@@ -42,6 +42,27 @@ __device__ inline bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds in the
+// instruction (it wakes when the phase completes), so idle waiters leave the
+// issue slots to other warps.
+__device__ inline bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ inline uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Waits for the phase with the given parity; gives up after `limit` polls
 // (each poll may suspend the thread for a short hardware-chosen time).
 __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {

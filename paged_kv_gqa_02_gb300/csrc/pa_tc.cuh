@@ -42,6 +42,21 @@ __device__ inline uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_
     return d;
 }
 
+// The same descriptor as two 32-bit words: the low word holds the start
+// address and leading byte offset, the high word the stride byte offset,
+// version and layout.  Advancing the start address by `off` bytes inside
+// one shared-memory window adds off >> 4 to the low word (the 14-bit field
+// cannot carry: shared addresses stay below 256 KB).
+__device__ inline uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ inline uint32_t desc_hi_sw128(uint32_t sbo) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ inline uint64_t make_desc(uint32_t lo, uint32_t hi) {
+    return (uint64_t(hi) << 32) | lo;
+}
+
 // Instruction descriptor for kind::f16 with f32 accumulation.
 //   ab_bf16: operands are bf16 (else f16); b_mn_major: B is MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool ab_bf16, bool b_mn_major) {
