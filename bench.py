@@ -183,7 +183,8 @@ def max_over_ranks(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as td
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if td.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     td.all_reduce(t, op=td.ReduceOp.MAX)
     return float(t.item())
 
