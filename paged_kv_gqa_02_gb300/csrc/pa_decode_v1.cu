@@ -43,7 +43,7 @@ constexpr int kCW = 8;                        // warps per CTA, each a partition
 constexpr int kThreadsV1 = kCW * 32;
 constexpr uint32_t kWaitLimit = 1u << 22;     // polls before a wait gives up
 constexpr int kMaxTiles = 64;                 // page tiles (half-stages) per CTA, at most
-constexpr int kMaxRing = 6;                   // page tiles in one warp's ring, at most
+constexpr int kMaxRing = 16;                  // page tiles in one warp's ring, at most
 constexpr int kSmemLimit = 232448;            // 227 KiB opt-in per CTA
 constexpr int kUnitCost = 2;                  // partition weight of a unit piece, in pages
 constexpr int kMinPartCost = 4;               // smallest share worth a warp, in cost units
@@ -222,16 +222,15 @@ __device__ inline void window_fill(LoadWindow& lw, const V1Params& a, int P) {
 
 // At most 224 registers a thread: 256 x 224 leaves room on the SM for one
 // combine CTA, which then starts (and locates its items) while this grid runs.
-template <typename T, int D, int P>
+template <typename T, int D, int P, int NT>
 __global__ void __maxnreg__(224)
     decode_v1(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const V1Params a) {
     constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
     constexpr int kHalves = D / 64;     // 128-byte swizzle spans per row
     constexpr int kTile = P * D * 2;    // one K (or V) page tile: a half-stage
-    constexpr int kTb = P / 8;          // 8-token blocks per page
-    constexpr int kKs = D / 16;         // k-steps of Q K^T
-    constexpr int kNt = D / 8;          // n-tiles of P V
+    constexpr int kMt = P / 16;         // 16-key row blocks of a page
+    constexpr int kKs = D / 16;         // k-steps of K Q^T; 16-dim row blocks of O^T
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -302,30 +301,39 @@ __global__ void __maxnreg__(224)
     };
     for (int hx = 0; hx < NH; ++hx) issue(hx);  // fill the ring
 
-    // ---- compute side ---------------------------------------------------------------
+    // ---- compute side: S^T = K Q^T and O^T += V^T P^T ---------------------------
+    // Keys (for S^T) and head dims (for O^T) are the MMA rows; the group's q
+    // heads are its 8-wide columns (NT column tiles), so a group of G <= 8
+    // heads wastes at most half of each MMA.
     const int g4 = lane >> 2, t4 = lane & 3;
+    const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: the matrix and row this lane addresses
     const int G = a.G;
-    // ldmatrix row addresses: lane supplies row (lane & 7) of matrix (lane >> 3);
-    // matrix m of a 32-dim block jj is the 16-byte chunk 4*jj + m (swizzled)
-    uint32_t koff[D / 32];
+    // Byte offset of (row, 16-byte chunk) in a page tile: two 64-dim halves of
+    // P rows of 128 bytes, chunks XOR-swizzled by row (128-byte swizzle).
+    auto swz = [](int row, int chunk) -> uint32_t {
+        return uint32_t((chunk >> 3) * (P * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    };
+    uint32_t offK[kKs], offV[kKs];
 #pragma unroll
-    for (int jj = 0; jj < D / 32; ++jj) {
-        const int chunk = 4 * jj + (lane >> 3), rr = lane & 7;
-        koff[jj] = (chunk >> 3) * (P * 128) + rr * 128 + (((chunk & 7) ^ rr) << 4);
+    for (int j = 0; j < kKs; ++j) {
+        offK[j] = swz((lm & 1) * 8 + lr, 2 * j + (lm >> 1));  // A = K rows (keys) x dims 16j..
+        offV[j] = swz((lm >> 1) * 8 + lr, 2 * j + (lm & 1));  // A = V^T rows (dims 16j..) x keys
     }
-    uint32_t qf[kKs][4], qn[kKs][4];
-    float o[kNt][4];
-    float sc[kTb][4];
-    // query rows of unit (b, g) straight into A fragments (rows >= G are 0)
-    auto load_q = [&](uint32_t (&dst)[kKs][4], int b, int g) {
-        const T* qb = static_cast<const T*>(a.q) + ((long long)b * a.Hq + g * G) * D;
+    uint32_t qb[NT][kKs][2], qn[NT][kKs][2];
+    float o[kKs][NT][4];
+    float sc[kMt][NT][4];
+    // B fragments of Q^T for unit (b, g): column n = q head nt*8 + g4 (0 past G)
+    auto load_q = [&](uint32_t (&dst)[NT][kKs][2], int b, int g) {
+        const T* qbase = static_cast<const T*>(a.q) + ((long long)b * a.Hq + g * G) * D;
 #pragma unroll
-        for (int ks = 0; ks < kKs; ++ks) {
-            const int col = 16 * ks + 2 * t4;
-            dst[ks][0] = g4 < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + g4 * D + col)) : 0u;
-            dst[ks][1] = g4 + 8 < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + (g4 + 8) * D + col)) : 0u;
-            dst[ks][2] = g4 < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + g4 * D + col + 8)) : 0u;
-            dst[ks][3] = g4 + 8 < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + (g4 + 8) * D + col + 8)) : 0u;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int h = nt * 8 + g4;
+            const uint32_t* row = reinterpret_cast<const uint32_t*>(qbase + (h < G ? h : 0) * D);
+#pragma unroll
+            for (int ks = 0; ks < kKs; ++ks) {
+                dst[nt][ks][0] = h < G ? __ldg(row + 8 * ks + t4) : 0u;
+                dst[nt][ks][1] = h < G ? __ldg(row + 8 * ks + 4 + t4) : 0u;
+            }
         }
     };
     load_q(qn, wk.b, wk.g);
@@ -335,20 +343,31 @@ __global__ void __maxnreg__(224)
         const int L = __ldg(a.context_lens + wk.b);
         const bool whole = (wk.pf == 0) && (wk.pe == wk.pb);
 #pragma unroll
-        for (int ks = 0; ks < kKs; ++ks)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) qf[ks][e] = qn[ks][e];
+            for (int ks = 0; ks < kKs; ++ks) {
+                qb[nt][ks][0] = qn[nt][ks][0];
+                qb[nt][ks][1] = qn[nt][ks][1];
+            }
         Walk nx = wk;  // the next piece, whose query rows load now
         walk_next_unit(nx, a, P);
         if (!nx.done) load_q(qn, nx.b, nx.g);
 
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        // running max and (lane-partial) denominator of heads nt*8 + 2*t4 + j
+        float mrun[NT][2], lrun[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < kNt; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+            mrun[nt][0] = mrun[nt][1] = -INFINITY;
+            lrun[nt][0] = lrun[nt][1] = 0.f;
+        }
+#pragma unroll
+        for (int dt = 0; dt < kKs; ++dt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) o[dt][nt][0] = o[dt][nt][1] = o[dt][nt][2] = o[dt][nt][3] = 0.f;
 
         for (int i = wk.pf; i < wk.pe; ++i) {
             const int ntok = min(P, L - i * P);
-            // ---- K tile: S = Q K^T, masked, online softmax
+            // ---- K tile: S^T = K Q^T, masked, online softmax
             bool ok = !timed_out;
             if (ok && !mbar_wait(&my_full[x % NH], (x / NH) & 1, kWaitLimit)) {
                 timed_out = true;
@@ -359,65 +378,85 @@ __global__ void __maxnreg__(224)
             if (valid) {
                 const uint32_t kb = smem_u32(my_tiles + size_t(x % NH) * kTile);
 #pragma unroll
-                for (int tb = 0; tb < kTb; ++tb) sc[tb][0] = sc[tb][1] = sc[tb][2] = sc[tb][3] = 0.f;
+                for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
-                for (int jj = 0; jj < D / 32; ++jj) {
+                    for (int nt = 0; nt < NT; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
 #pragma unroll
-                    for (int tb = 0; tb < kTb; ++tb) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(kb + tb * 1024 + koff[jj], b0, b1, b2, b3);
-                        mma_16816<kBf>(sc[tb], qf[2 * jj], b0, b1);
-                        mma_16816<kBf>(sc[tb], qf[2 * jj + 1], b2, b3);
+                for (int ks = 0; ks < kKs; ++ks) {
+#pragma unroll
+                    for (int mt = 0; mt < kMt; ++mt) {
+                        uint32_t ka[4];
+                        ldsm_x4(kb + mt * 2048 + offK[ks], ka[0], ka[1], ka[2], ka[3]);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) mma_16816<kBf>(sc[mt][nt], ka, qb[nt][ks][0], qb[nt][ks][1]);
                     }
                 }
             }
             __syncwarp();
             if (!timed_out) issue(x + NH);  // the K slot is free again
             ++x;
+            uint32_t ph[kMt][NT][2], pl[kMt][NT][2];  // P^T as B fragments: high parts, remainders
             if (valid) {
-                float mx0 = -INFINITY, mx1 = -INFINITY;
+                float mx[NT][2];
 #pragma unroll
-                for (int tb = 0; tb < kTb; ++tb) {
-                    const int tok = tb * 8 + 2 * t4;
+                for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        sc[tb][e] *= a.scale_log2;
-                        if (tok + (e & 1) >= ntok) sc[tb][e] = -INFINITY;
+                for (int mt = 0; mt < kMt; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int tok = 16 * mt + g4 + ((e & 2) ? 8 : 0);
+                            const float v = tok < ntok ? sc[mt][nt][e] * a.scale_log2 : -INFINITY;
+                            sc[mt][nt][e] = v;
+                            mx[nt][e & 1] = fmaxf(mx[nt][e & 1], v);
+                        }
+                bool same = true;
+                float al[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float v = mx[nt][j];
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                        const float mn = fmaxf(mrun[nt][j], v);
+                        al[nt][j] = ex2(mrun[nt][j] - mn);  // m = -inf -> 0
+                        same = same && al[nt][j] == 1.f;
+                        mrun[nt][j] = mn;
+                        lrun[nt][j] *= al[nt][j];
                     }
-                    mx0 = fmaxf(mx0, fmaxf(sc[tb][0], sc[tb][1]));
-                    mx1 = fmaxf(mx1, fmaxf(sc[tb][2], sc[tb][3]));
-                }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);  // m = -inf -> 0
-                m0 = mn0;
-                m1 = mn1;
-                float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-                for (int tb = 0; tb < kTb; ++tb) {
-                    sc[tb][0] = ex2(sc[tb][0] - mn0);
-                    sc[tb][1] = ex2(sc[tb][1] - mn0);
-                    sc[tb][2] = ex2(sc[tb][2] - mn1);
-                    sc[tb][3] = ex2(sc[tb][3] - mn1);
-                    ps0 += sc[tb][0] + sc[tb][1];
-                    ps1 += sc[tb][2] + sc[tb][3];
-                }
-                l0 = l0 * al0 + ps0;
-                l1 = l1 * al1 + ps1;
-                if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
+                for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
-                    for (int nt = 0; nt < kNt; ++nt) {
-                        o[nt][0] *= al0;
-                        o[nt][1] *= al0;
-                        o[nt][2] *= al1;
-                        o[nt][3] *= al1;
+                    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            sc[mt][nt][e] = ex2(sc[mt][nt][e] - mrun[nt][e & 1]);
+                            lrun[nt][e & 1] += sc[mt][nt][e];
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            uint32_t hi, lo;
+                            split_hi_lo<T>(sc[mt][nt][2 * j], sc[mt][nt][2 * j + 1], hi, lo);
+                            ph[mt][nt][j] = movm_trans(hi);
+                            pl[mt][nt][j] = movm_trans(lo);
+                        }
                     }
+                if (!__all_sync(0xffffffffu, same)) {
+#pragma unroll
+                    for (int dt = 0; dt < kKs; ++dt)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            o[dt][nt][0] *= al[nt][0];
+                            o[dt][nt][1] *= al[nt][1];
+                            o[dt][nt][2] *= al[nt][0];
+                            o[dt][nt][3] *= al[nt][1];
+                        }
                 }
             }
-            // ---- V tile: O += P V
+            // ---- V tile: O^T += V^T P^T
             ok = !timed_out;
             if (ok && !mbar_wait(&my_full[x % NH], (x / NH) & 1, kWaitLimit)) {
                 timed_out = true;
@@ -438,56 +477,69 @@ __global__ void __maxnreg__(224)
                 }
                 const uint32_t vb = smem_u32(vt);
 #pragma unroll
-                for (int tb = 0; tb < kTb; ++tb) {
-                    uint32_t pa[4];
-                    split_hi_lo<T>(sc[tb][0], sc[tb][1], pa[0], pa[2]);
-                    split_hi_lo<T>(sc[tb][2], sc[tb][3], pa[1], pa[3]);
+                for (int kk = 0; kk < kMt; ++kk)
 #pragma unroll
-                    for (int jj = 0; jj < D / 32; ++jj) {
-                        uint32_t v[4];
-                        ldsm_x4_t(vb + tb * 1024 + koff[jj], v[0], v[1], v[2], v[3]);
+                    for (int dt = 0; dt < kKs; ++dt) {
+                        uint32_t va[4];
+                        ldsm_x4_t(vb + kk * 2048 + offV[dt], va[0], va[1], va[2], va[3]);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) mma_16816<kBf>(o[4 * jj + q], pa, v[q], v[q]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma_16816<kBf>(o[dt][nt], va, ph[kk][nt][0], ph[kk][nt][1]);
+                            mma_16816<kBf>(o[dt][nt], va, pl[kk][nt][0], pl[kk][nt][1]);
+                        }
                     }
-                }
             }
             __syncwarp();
             if (!timed_out) issue(x + NH);  // the V slot is free again
             ++x;
         }
 
-        // ---- the piece's result: final output, or a partial for the combine
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        // ---- the piece's result: final output, or a partial for the combine.
+        // Lane (g4, t4) holds dims 16*dt + g4 (+8) of heads nt*8 + 2*t4 + j.
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float v = lrun[nt][j];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                lrun[nt][j] = v;
+            }
         if (whole) {
-            const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
             float* ob = a.out + ((long long)wk.b * a.Hq + wk.g * G) * D;
 #pragma unroll
-            for (int nt = 0; nt < kNt; ++nt) {
-                const int col = nt * 8 + 2 * t4;
-                if (g4 < G)
-                    *reinterpret_cast<float2*>(ob + g4 * D + col) = make_float2(o[nt][0] * i0, o[nt][1] * i0);
-                if (g4 + 8 < G)
-                    *reinterpret_cast<float2*>(ob + (g4 + 8) * D + col) =
-                        make_float2(o[nt][2] * i1, o[nt][3] * i1);
-            }
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int h = nt * 8 + 2 * t4 + j;
+                    if (h < G) {
+                        const float inv = lrun[nt][j] > 0.f ? 1.f / lrun[nt][j] : 0.f;
+#pragma unroll
+                        for (int dt = 0; dt < kKs; ++dt) {
+                            ob[h * D + 16 * dt + g4] = o[dt][nt][j] * inv;
+                            ob[h * D + 16 * dt + g4 + 8] = o[dt][nt][2 + j] * inv;
+                        }
+                    }
+                }
         } else {
             const long long slot = part + (long long)wk.b * a.Hkv + wk.g;
             float* accp = a.ws_acc + slot * G * D;
             float* ml = a.ws_ml + slot * G * 2;
 #pragma unroll
-            for (int nt = 0; nt < kNt; ++nt) {
-                const int col = nt * 8 + 2 * t4;
-                if (g4 < G) *reinterpret_cast<float2*>(accp + g4 * D + col) = make_float2(o[nt][0], o[nt][1]);
-                if (g4 + 8 < G)
-                    *reinterpret_cast<float2*>(accp + (g4 + 8) * D + col) = make_float2(o[nt][2], o[nt][3]);
-            }
-            if (t4 == 0) {
-                if (g4 < G) *reinterpret_cast<float2*>(ml + g4 * 2) = make_float2(m0, l0);
-                if (g4 + 8 < G) *reinterpret_cast<float2*>(ml + (g4 + 8) * 2) = make_float2(m1, l1);
-            }
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int h = nt * 8 + 2 * t4 + j;
+                    if (h < G) {
+#pragma unroll
+                        for (int dt = 0; dt < kKs; ++dt) {
+                            accp[h * D + 16 * dt + g4] = o[dt][nt][j];
+                            accp[h * D + 16 * dt + g4 + 8] = o[dt][nt][2 + j];
+                        }
+                        if (g4 == 0) *reinterpret_cast<float2*>(ml + h * 2) = make_float2(mrun[nt][j], lrun[nt][j]);
+                    }
+                }
         }
         wk = nx;
     }
@@ -496,109 +548,84 @@ __global__ void __maxnreg__(224)
         for (int s = 0; s < NH; ++s) mbar_wait(&my_full[s], ((x + s) / NH) & 1, 1024);
 }
 
-// Merges the pieces of units that span several parts.  A persistent grid of
-// one CTA per SM, resident beside the partial kernel (which it waits for
-// through programmatic dependent launch), gives each warp (q head, sequence)
-// items in turn.  A warp locates an item's pieces from the lengths alone (a
-// lane-parallel prefix over the sequences before it) before the partial
-// kernel ends; only the pieces' loads come after.  The maxima and
-// denominators are reduced by fixed shuffle trees, so the result does not
-// depend on timing.  At most 64 registers a thread (D threads, 1024/D CTAs an
-// SM), so the CTA fits beside a partial CTA of 256 x 224 registers.
+// Merges the pieces of units that span several parts: one CTA per (sequence,
+// q head), one thread per output dim.  The CTA locates its pieces from the
+// lengths alone (a lane-parallel prefix over the sequences) before it waits
+// for the partial kernel through programmatic dependent launch; after the
+// wait, the (m, l) pairs of up to 32 pieces (one per lane) and their
+// accumulators (one per thread and piece) are loaded together, so a merge
+// costs about one L2 round trip.  Maxima and denominators are reduced by
+// fixed shuffle trees and the accumulators are summed in ascending part
+// order, so the result does not depend on timing.  At most 64 registers a
+// thread (1024/D CTAs an SM), so the CTAs that start while the partial kernel
+// runs fit beside its 256 x 224-register CTA.
 template <int D>
 __global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int P) {
-    constexpr int kWarps = D / 32;
-    constexpr int kVpl = D / 32;  // output dims per lane
-    __shared__ long long sh_T;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    constexpr int kBatch = 32;  // pieces loaded together
+    const int lane = threadIdx.x & 31, d = threadIdx.x;
+    const int item = blockIdx.x;  // b * Hq + h
+    const int b = item / a.Hq, h = item % a.Hq, g = h / a.G, r = h % a.G;
+    const int unit = b * a.Hkv + g;
     const int W = a.unit_cost;
-    const int n_items = a.Hq * a.B;
-    if (wid == 0) {
-        long long tot = 0;
-        for (int x = lane; x < a.B; x += 32) {
-            const int pg = seq_pages(a.context_lens, x, P, a.max_len);
-            tot += pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
-        }
-        tot = warp_sum_ll(tot);
-        if (lane == 0) sh_T = tot;
+    long long T = 0, pre = 0;
+    for (int x = lane; x < a.B; x += 32) {
+        const int pg = seq_pages(a.context_lens, x, P, a.max_len);
+        const long long c = pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
+        T += c;
+        if (x < b) pre += c;
     }
-    __syncthreads();
-    const long long T = sh_T;
+    T = warp_sum_ll(T);
+    pre = warp_sum_ll(pre);
+    const int pb = seq_pages(a.context_lens, b, P, a.max_len);
     const long long n = parts_in_use(T > 0 ? T : 1, a);
-    bool waited = false;
-    for (int it = blockIdx.x * kWarps + wid; it < n_items; it += gridDim.x * kWarps) {
-        const int b = it / a.Hq, h = it % a.Hq, g = h / a.G, r = h % a.G;
-        const int unit = b * a.Hkv + g;
-        // ---- locate the item's pieces
-        long long pre = 0;
-        for (int x = lane; x < b; x += 32) {
-            const int pg = seq_pages(a.context_lens, x, P, a.max_len);
-            pre += pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
-        }
-        pre = warp_sum_ll(pre);
-        const int pb = seq_pages(a.context_lens, b, P, a.max_len);
-        int c0 = 0, np = 0;
-        if (pb > 0) {  // the unit's pages sit at cost positions [p0, p0 + pb)
-            const long long p0 = pre + (long long)g * (pb + W) + W;
-            c0 = int(((p0 + 1) * n - 1) / T);  // part v owns [v*T/n, (v+1)*T/n)
-            const int c1 = int(((p0 + pb) * n - 1) / T);
-            np = c1 > c0 ? c1 - c0 + 1 : 0;  // 0: finished inside one part
-        }
-        if (!waited) {  // the partial kernel's pieces are complete from here on
-            pdl_wait_primary();
-            waited = true;
-        }
-        float* o = a.out + ((long long)b * a.Hq + h) * D + lane * kVpl;
-        if (pb == 0) {
-#pragma unroll
-            for (int e = 0; e < kVpl; ++e) o[e] = 0.f;
-            if (h == 0 && lane == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
-            continue;
-        }
-        if (np == 0) continue;
-        // ---- merge; parts between c0 and c1 whose share is empty (possible when
-        // T < n) wrote nothing: their weight is 0 and their rows are never used
-        float M = -INFINITY;
-        for (int x = lane; x < np; x += 32) {
-            const long long cc = c0 + x;
-            if (cc * T / n != (cc + 1) * T / n) M = fmaxf(M, a.ws_ml[((cc + unit) * a.G + r) * 2]);
-        }
-        M = warp_max(M);
-        float den = 0.f, num[kVpl];
-#pragma unroll
-        for (int e = 0; e < kVpl; ++e) num[e] = 0.f;
-        for (int x0 = 0; x0 < np; x0 += 32) {
-            const long long cc = c0 + x0 + lane;
-            float wgt = 0.f;
-            if (x0 + lane < np && cc * T / n != (cc + 1) * T / n) {
-                const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((cc + unit) * a.G + r) * 2);
-                if (ml.x != -INFINITY) {
-                    wgt = ex2(ml.x - M);
-                    den = fmaf(wgt, ml.y, den);
-                }
-            }
-            const int cnt = min(32, np - x0);
-            const float* accp = a.ws_acc + ((long long)(c0 + x0 + unit) * a.G + r) * D + lane * kVpl;
-#pragma unroll 8
-            for (int j = 0; j < cnt; ++j) {
-                const float wj = __shfl_sync(0xffffffffu, wgt, j);
-                float v[kVpl];
-                if constexpr (kVpl == 4) {
-                    const float4 t = *reinterpret_cast<const float4*>(accp + (long long)j * a.G * D);
-                    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-                } else {
-                    const float2 t = *reinterpret_cast<const float2*>(accp + (long long)j * a.G * D);
-                    v[0] = t.x; v[1] = t.y;
-                }
-#pragma unroll
-                for (int e = 0; e < kVpl; ++e) num[e] = wj != 0.f ? fmaf(wj, v[e], num[e]) : num[e];
-            }
-        }
-        den = warp_sum(den);
-#pragma unroll
-        for (int e = 0; e < kVpl; ++e) o[e] = den > 0.f ? num[e] / den : 0.f;
+    long long c0 = 0;
+    int np = 0;
+    if (pb > 0) {  // the unit's pages sit at cost positions [p0, p0 + pb)
+        const long long p0 = pre + (long long)g * (pb + W) + W;
+        c0 = ((p0 + 1) * n - 1) / T;  // part v owns [v*T/n, (v+1)*T/n)
+        const long long c1 = ((p0 + pb) * n - 1) / T;
+        np = c1 > c0 ? int(c1 - c0 + 1) : 0;  // 0: finished inside one part
     }
-    if (!waited) pdl_wait_primary();
+    pdl_wait_primary();  // the partial kernel's pieces are complete from here on
+    float* o = a.out + (long long)item * D + d;
+    if (pb == 0) {
+        *o = 0.f;
+        if (h == 0 && d == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
+        return;
+    }
+    if (np == 0) return;
+    // Parts between c0 and c1 whose share is empty (possible when T < n) wrote
+    // nothing: their weight is 0 and their rows are never used.
+    float M = -INFINITY, den = 0.f, num = 0.f;
+    for (int x0 = 0; x0 < np; x0 += kBatch) {
+        const int cnt = min(kBatch, np - x0);
+        float mj = -INFINITY, lj = 0.f;
+        if (lane < cnt) {
+            const long long cc = c0 + x0 + lane;
+            if (cc * T / n != (cc + 1) * T / n) {
+                const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((cc + unit) * a.G + r) * 2);
+                mj = ml.x;
+                lj = ml.y;
+            }
+        }
+        const float* accp = a.ws_acc + ((c0 + x0 + unit) * a.G + r) * D + d;
+        float v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) v[j] = j < cnt ? accp[(long long)j * a.G * D] : 0.f;
+        const float Mn = fmaxf(M, warp_max(mj));
+        if (Mn == -INFINITY) continue;  // no key so far
+        const float sc = ex2(M - Mn);   // M = -inf -> 0
+        const float wj = mj == -INFINITY ? 0.f : ex2(mj - Mn);
+        den = den * sc + warp_sum(wj * lj);
+        num *= sc;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wj, j);
+            num = w != 0.f ? fmaf(w, v[j], num) : num;
+        }
+        M = Mn;
+    }
+    *o = den > 0.f ? num / den : 0.f;
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -629,25 +656,32 @@ size_t smem_bytes(int D, int P, int ntiles) {
     return 1024 + size_t(ntiles) * P * D * 2 + v1_fixed_bytes();
 }
 
+template <typename T, int D, int P, int NT>
+cudaError_t launch_partial(const CUtensorMap& k, const CUtensorMap& v, const V1Params& a, int n_ctas,
+                           cudaStream_t st) {
+    auto kern = decode_v1<T, D, P, NT>;
+    static bool configured = false;  // benign race: every caller sets the same value
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<n_ctas, kThreadsV1, smem_bytes(D, P, a.ntiles), st>>>(k, v, a);
+    return cudaGetLastError();
+}
+
 template <typename T, int D, int P>
 cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Params& a, int n_ctas,
                          int phases, cudaStream_t st) {
     if (phases & 1) {
-        auto kern = decode_v1<T, D, P>;
-        static bool configured = false;  // benign race: every caller sets the same value
-        if (!configured) {
-            cudaError_t e =
-                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-            if (e != cudaSuccess) return e;
-            configured = true;
-        }
-        kern<<<n_ctas, kThreadsV1, smem_bytes(D, P, a.ntiles), st>>>(k, v, a);
-        cudaError_t e = cudaGetLastError();
+        // one 8-wide column tile of q heads when the group fits, else two
+        cudaError_t e = a.G <= 8 ? launch_partial<T, D, P, 1>(k, v, a, n_ctas, st)
+                                 : launch_partial<T, D, P, 2>(k, v, a, n_ctas, st);
         if (e != cudaSuccess) return e;
     }
     if (!(phases & 2)) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_ctas);
+    cfg.gridDim = dim3(unsigned(a.B) * unsigned(a.Hq));
     cfg.blockDim = dim3(D);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

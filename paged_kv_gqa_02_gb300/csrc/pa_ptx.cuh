@@ -154,6 +154,14 @@ __device__ inline void mma_16816(float* c, const uint32_t* a, uint32_t b0, uint3
     }
 }
 
+// Transposes an 8x8 matrix of 16-bit elements held in the MMA fragment
+// layout (lane 4r + c holds row r, columns 2c and 2c + 1).
+__device__ inline uint32_t movm_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 template <bool kBf16>
 __device__ inline void mma_1688(float* c, uint32_t a0, uint32_t a1, uint32_t b0) {
     if constexpr (kBf16) {
