@@ -5,8 +5,8 @@ One step = one call of the hot path on one batch: pa_decode (split partials
 + combine) on the ragged continuous-batching decode batch (16 sequences,
 32 q / 8 kv heads, head_dim 128, 32-token pages, bf16) unless --workload
 names another.  Inputs are device-resident; consecutive calls rotate over R
-copies of them whose total footprint is at least 3x the L2 size, so every
-call reads K/V from HBM.  The K timed steps are replays of a CUDA graph of
+disjoint sets of physical pages of one pool (and R copies of q) whose total
+footprint is at least 3x the L2 size, so every call reads K/V from HBM.  The K timed steps are replays of a CUDA graph of
 calls, timed with CUDA events on the launching stream.
 
 value = algorithmic bytes per call (K+V once per kv head, Q, O as f32)
@@ -192,23 +192,49 @@ def max_over_ranks(x: float, world: int) -> float:
 # --------------------------------------------------------------- GPU arm --
 
 class Rotation:
-    """R device copies of one problem's inputs (pools stacked, tables shifted)."""
+    """R rotation steps over one page pool of the workload's own layout.
+
+    Step i reads its own set of physical pages, disjoint from every other
+    step's and holding a copy of the problem's page data, and its own copy of
+    q, so no call finds its K/V or q in L2 from an earlier call while the
+    results stay the same.  The pool keeps the workload's page count unless
+    R sets of used pages need more; the sets are drawn from one seeded
+    Fisher-Yates shuffle of the pool (consecutive page ids when the workload's
+    table is the identity)."""
+
+    TID_ROTATION = 5  # generator stream of the rotation's page shuffle
 
     def __init__(self, wl, inp, R, ops, torch):
+        import numpy as np
+        from paged_kv_gqa_02_gb300 import inputs
         base = ops.device_inputs(inp, wl)
-        npg = int(inp["num_pages"])
+        bt0 = np.asarray(inp["block_tables"])
+        npg0 = int(inp["num_pages"])
+        used = np.unique(bt0[bt0 >= 0]).astype(np.int64)
+        U = len(used)
+        pool = max(npg0, R * U)
+        order = (inputs.fisher_yates(pool, inputs.stream_seed(wl.seed, self.TID_ROTATION))
+                 if wl.shuffle else np.arange(pool, dtype=np.int64))
+        k0, v0 = base["k_cache"], base["v_cache"]
+        self.k = torch.zeros((pool,) + tuple(k0.shape[1:]), dtype=k0.dtype, device="cuda")
+        self.v = torch.zeros_like(self.k)
+        src = torch.as_tensor(used, device="cuda")
         self.R = R
-        self.k = base["k_cache"].repeat(R, 1, 1, 1)
-        self.v = base["v_cache"].repeat(R, 1, 1, 1)
+        self.pool_pages = pool
         self.q = [base["q"].clone() for _ in range(R)]
         self.bt = []
         for i in range(R):
-            t = base["block_tables"].clone()
-            t[t >= 0] += i * npg
-            self.bt.append(t)
+            dst = np.asarray(order[i * U:(i + 1) * U], dtype=np.int64)
+            dst_t = torch.as_tensor(dst, device="cuda")
+            self.k[dst_t] = k0[src]
+            self.v[dst_t] = v0[src]
+            remap = np.full(npg0, -1, dtype=np.int64)
+            remap[used] = dst
+            t = np.where(bt0 >= 0, remap[np.clip(bt0, 0, None)], bt0).astype(np.int32)
+            self.bt.append(torch.as_tensor(t, device="cuda"))
         self.cl = base["context_lens"]
         self.cu = base["cu_q_lens"]
-        self.params = ops.params_for(wl, num_pages=R * npg)
+        self.params = ops.params_for(wl, num_pages=pool)
         self.out = torch.empty((wl.total_q, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
                                device="cuda")
 
@@ -360,7 +386,7 @@ def measure_workload(wl, ops, torch, K, W, world, l2, hbm_peak, flop_peak, clock
     inp = wl.make_inputs()
     R = rotation_copies(wl, l2)
     rot = Rotation(wl, inp, R, ops, torch)
-    res = {"workload": wl.name, "rotation_copies": R}
+    res = {"workload": wl.name, "rotation_copies": R, "pool_pages": rot.pool_pages}
     if wl.kind == "decode":
         calls, launches, S = decode_calls(rot, ops, torch)
         ms, t0, t1 = time_graph(torch, calls, K, W, world)
@@ -454,8 +480,8 @@ def run_ours(args):
                    "head_dim": wl.head_dim, "page_size": wl.page_size,
                    "context_tokens": sum(wl.context_lens), "num_splits": main.get("num_splits"),
                    "algorithmic_bytes_per_call": wl.algorithmic_bytes(),
-                   "l2": f"inputs larger than L2: rotation over {main['rotation_copies']} copies "
-                         f"(>= 3x the {l2 // 2**20} MiB L2)",
+                   "l2": f"inputs larger than L2: rotation over {main['rotation_copies']} disjoint page "
+                         f"sets of one {main['pool_pages']}-page pool (>= 3x the {l2 // 2**20} MiB L2)",
                    "timing": "CUDA graph replays, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,

@@ -5,28 +5,31 @@
 // a call is the ordered list of (sequence, kv head) units, unit (b, g) made of
 // the pages of sequence b read for kv head g.  In a cost space where each
 // unit occupies unit_cost + pages positions (unit_cost stands for the fixed
-// work of a unit piece: its query rows and its result), the grid's
-// n = min(CTAs x 8 warps, T / kMinPartCost) parts take equal contiguous shares
-// [v*T/n, (v+1)*T/n).  Every warp therefore moves about the same
-// number of bytes whatever the mix of context lengths, and the grid does not
-// depend on device data.  A warp finishes a unit that lies inside its share;
-// the pieces of the other units go to the workspace and a combine kernel,
-// launched with programmatic dependent launch, merges them in ascending part
-// order (split-KV combine, crucible README "Split-position attention":
-// rescale by exp(m_i - m_max), then merge).
+// work of a unit piece: its query row and its result), the n CTAs in use
+// (all of the persistent grid unless the call is tiny) take equal contiguous
+// shares [c*T/n, (c+1)*T/n), and the 8 warps of a CTA split its share the
+// same way.  Every warp therefore moves about the same number of bytes
+// whatever the mix of context lengths, and the grid does not depend on
+// device data.  A warp finishes a unit that lies inside its part.  When the
+// group's q heads fit one 8-wide MMA column tile, the warps of a CTA then
+// merge the pieces they share in shared memory, so a unit leaves at most one
+// piece per CTA; otherwise each warp writes its pieces.  A combine kernel,
+// launched with programmatic dependent launch, merges the pieces of units
+// that span several parts in ascending part order (split-KV combine, crucible
+// README "Split-position attention": rescale by exp(m_i - m_max), then merge).
 //
-// Each warp reads the block table of its share ahead (32 pages at a time,
+// Each warp reads the block table of its part ahead (32 pages at a time,
 // one lane per page) and issues its own TMA copies of each page's K and V
 // tiles (one kv head, all page_size slots, 128B-swizzled) into its own ring
 // of half-stages guarded by mbarriers, refilling a slot as soon as it has
-// used it; no warp waits for another.  Each warp streams its pages: S = Q K^T with
-// mma.sync m16n8k16 (the group's q heads padded to 16 rows), an online softmax
-// in base 2 (crucible results, the online-softmax experiment), and O += P V
-// with m16n8k16 whose A operand is built from the S accumulator in registers.
-// The probabilities are split into a 16-bit high part and a 16-bit remainder
-// stacked along k (the V fragment is passed twice), keeping 16 (bf16) or 22
-// (f16) bits of them: one 16-bit rounding alone moves small outputs by more
-// than 1% of their size.
+// used it; no warp waits for another.  Each warp streams its pages: S^T = K Q^T
+// with mma.sync m16n8k16 (keys as the MMA rows, the group's q heads as its
+// 8-wide columns), an online softmax in base 2 (crucible results, the
+// online-softmax experiment), and O^T += V^T P^T with P^T moved into the B
+// operand layout by movmatrix.  The probabilities are split into a 16-bit
+// high part and a 16-bit remainder, both multiplied by V, keeping 16 (bf16)
+// or 22 (f16) bits of them: one 16-bit rounding alone moves small outputs by
+// more than 1% of their size.
 #include <cudaTypedefs.h>
 
 #include <type_traits>
@@ -46,7 +49,8 @@ constexpr int kMaxTiles = 64;                 // page tiles (half-stages) per CT
 constexpr int kMaxRing = 16;                  // page tiles in one warp's ring, at most
 constexpr int kSmemLimit = 232448;            // 227 KiB opt-in per CTA
 constexpr int kUnitCost = 2;                  // partition weight of a unit piece, in pages
-constexpr int kMinPartCost = 4;               // smallest share worth a warp, in cost units
+constexpr int kMinCtaCost = 3;                // smallest share worth a CTA, in cost units
+constexpr int kCtaMergeMaxShare = 16;         // CTA merge only while CTA shares average at most this
 
 struct V1Params {
     const void* q;  // [B*Hq][D]
@@ -58,7 +62,8 @@ struct V1Params {
     uint32_t* dev_status;
     int32_t B, Hq, Hkv, G, num_pages, max_blocks, max_len;
     float scale_log2;
-    int32_t n_parts, ntiles, head_first, unit_cost;
+    int32_t n_ctas, ntiles, head_first, unit_cost;
+    int32_t cta_pieces;  // 1: the group fits one MMA column tile, so small calls merge per CTA
 };
 
 // A warp's position in its share of the cost space.
@@ -194,12 +199,13 @@ __device__ inline void split_hi_lo(float x, float y, uint32_t& hi, uint32_t& lo)
     }
 }
 
-// Part v of the partition runs on CTA v % n_ctas, warp v / n_ctas, so that
-// when fewer parts than warps are in use every SM still gets a share.  The
-// number of parts in use is a function of the inputs alone.
-__device__ inline long long parts_in_use(long long T, const V1Params& a) {
-    const long long want = (T + kMinPartCost - 1) / kMinPartCost;
-    return want < 1 ? 1 : (want < a.n_parts ? want : a.n_parts);
+// CTAs that take a share: all of them unless the call is so small that a
+// share would fall below kMinCtaCost.  A function of the inputs and the grid
+// alone.  CTA c owns [c*T/n, (c+1)*T/n) of the cost space; its warp w owns
+// the matching eighth, part c*8 + w of the n*8 warp parts.
+__device__ inline long long ctas_in_use(long long T, long long grid) {
+    const long long want = (T + kMinCtaCost - 1) / kMinCtaCost;
+    return want < 1 ? 1 : (want < grid ? want : grid);
 }
 
 // The load side of a warp: lane l holds page base + l of the warp's share
@@ -231,6 +237,9 @@ __global__ void __maxnreg__(224)
     constexpr int kTile = P * D * 2;    // one K (or V) page tile: a half-stage
     constexpr int kMt = P / 16;         // 16-key row blocks of a page
     constexpr int kKs = D / 16;         // k-steps of K Q^T; 16-dim row blocks of O^T
+    // One column tile: warps of a CTA merge their pieces in shared memory.
+    // Two: each warp's non-whole pieces go to the workspace.
+    constexpr bool kCtaMerge = NT == 1;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -239,21 +248,27 @@ __global__ void __maxnreg__(224)
 
     pdl_launch_dependents();
 
-    // ---- this warp's share of the cost space ------------------------------------
+    // ---- this CTA's share of the cost space, and this warp's part of it ---------
     const long long cost = total_cost(a, P);
-    const long long n_used = parts_in_use(cost, a);
-    const long long part = (long long)warp * gridDim.x + blockIdx.x;
-    if (part >= n_used) return;
-    // The CTA's pool of page tiles is divided among its active warps
-    // (warps 0 .. active-1), so a CTA with few parts keeps more pages in
-    // flight per part.
-    const int active = int((n_used - blockIdx.x + gridDim.x - 1) / gridDim.x);
-    const int NH = min(a.ntiles / active, kMaxRing);
+    const long long n_cta = ctas_in_use(cost, gridDim.x);
+    if (blockIdx.x >= n_cta) return;  // the whole CTA, before any CTA barrier
+    const long long n = n_cta * kCW;
+    const long long part = (long long)blockIdx.x * kCW + warp;
+    const long long cta_s = (long long)blockIdx.x * cost / n_cta, cta_e = (blockIdx.x + 1) * cost / n_cta;
+    // Small calls (short shares, few pages a warp) merge the warps' pieces in
+    // the CTA, so the combine sees one piece per CTA; larger ones leave each
+    // warp's pieces to the combine.  Uniform over the grid.
+    const bool cta_merge = kCtaMerge && cost <= (long long)kCtaMergeMaxShare * n_cta;
+    const int NH = min(a.ntiles / kCW, kMaxRing);
     uint8_t* my_tiles = base + size_t(warp) * NH * kTile;  // [NH][kTile]
     int* my_page = reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile) + warp * NH;
     uint64_t* my_full =
         reinterpret_cast<uint64_t*>(reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile) + kMaxTiles) +
         warp * NH;
+    __shared__ int s_unit[kCW][2];  // CTA merge: unit of each warp's pieces (-1: none)
+    __shared__ int s_inside[kCW][2];
+    __shared__ float s_w[kCtaMerge ? 8 : 1][2 * kCW];  // CTA merge: weight of each entry, per head
+    __shared__ float s_md[kCtaMerge ? 8 : 1][2];       // CTA merge: max and denominator, per head
     if (lane == 0) {
         for (int s = 0; s < NH; ++s) mbar_init(&my_full[s], 1);
         mbar_fence_init();
@@ -261,14 +276,17 @@ __global__ void __maxnreg__(224)
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
         }
+        s_unit[warp][0] = s_unit[warp][1] = -1;
     }
     __syncwarp();
-    Walk wk = walk_start(a, P, part * cost / n_used, (part + 1) * cost / n_used);
-    if (wk.done) return;
+    Walk wk = walk_start(a, P, part * cost / n, (part + 1) * cost / n);
 
     // ---- load side: issue half-stage x (page x/2 of the share; K, then V)
+    // K/V are read once per call: evict-first keeps the kernel's code, the
+    // lengths, tables and workspace in L2 while the pages stream through.
+    const uint64_t kv_policy = l2_policy_evict_first();
     LoadWindow lw{wk, wk.pf, 0, 0, 0, -1};
-    window_fill(lw, a, P);
+    if (!wk.done) window_fill(lw, a, P);
     bool timed_out = false;
     auto issue = [&](int hx) {
         const int j = hx >> 1;
@@ -293,13 +311,14 @@ __global__ void __maxnreg__(224)
                 const int xc = a.head_first ? g : 0, yc = a.head_first ? 0 : g;
 #pragma unroll
                 for (int hh = 0; hh < kHalves; ++hh)
-                    tma_load_4d(dst + hh * P * 128, (hx & 1) ? &tmV : &tmK, &my_full[slot], 64 * hh, xc, yc,
-                                pg);
+                    tma_load_4d_hint(dst + hh * P * 128, (hx & 1) ? &tmV : &tmK, &my_full[slot], 64 * hh, xc,
+                                     yc, pg, kv_policy);
             }
         }
         __syncwarp();
     };
-    for (int hx = 0; hx < NH; ++hx) issue(hx);  // fill the ring
+    if (!wk.done)
+        for (int hx = 0; hx < NH; ++hx) issue(hx);  // fill the ring
 
     // ---- compute side: S^T = K Q^T and O^T += V^T P^T ---------------------------
     // Keys (for S^T) and head dims (for O^T) are the MMA rows; the group's q
@@ -336,8 +355,14 @@ __global__ void __maxnreg__(224)
             }
         }
     };
-    load_q(qn, wk.b, wk.g);
+    if (!wk.done) load_q(qn, wk.b, wk.g);
     int x = 0;  // half-stage number
+    // CTA merge (one q-head column tile): the share's first piece, when it is
+    // not whole and other units follow, waits here; its last non-whole piece
+    // stays in o / mrun / lrun.
+    float of[kKs][4], mf[2], lf[2];
+    int first_unit = -1, first_inside = 0, last_unit = -1, last_inside = 0;
+    float mrun[NT][2], lrun[NT][2];
 
     while (!wk.done) {
         const int L = __ldg(a.context_lens + wk.b);
@@ -354,7 +379,6 @@ __global__ void __maxnreg__(224)
         if (!nx.done) load_q(qn, nx.b, nx.g);
 
         // running max and (lane-partial) denominator of heads nt*8 + 2*t4 + j
-        float mrun[NT][2], lrun[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             mrun[nt][0] = mrun[nt][1] = -INFINITY;
@@ -377,10 +401,13 @@ __global__ void __maxnreg__(224)
             const bool valid = ok && my_page[x % NH] >= 0;
             if (valid) {
                 const uint32_t kb = smem_u32(my_tiles + size_t(x % NH) * kTile);
+                float s2[kMt][NT][4];  // one column tile: odd k-steps in a second accumulator (shorter chains)
 #pragma unroll
                 for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[mt][nt][e] = s2[mt][nt][e] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < kKs; ++ks) {
 #pragma unroll
@@ -388,9 +415,17 @@ __global__ void __maxnreg__(224)
                         uint32_t ka[4];
                         ldsm_x4(kb + mt * 2048 + offK[ks], ka[0], ka[1], ka[2], ka[3]);
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma_16816<kBf>(sc[mt][nt], ka, qb[nt][ks][0], qb[nt][ks][1]);
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_16816<kBf>((NT == 1 && (ks & 1)) ? s2[mt][nt] : sc[mt][nt], ka, qb[nt][ks][0],
+                                           qb[nt][ks][1]);
                     }
                 }
+#pragma unroll
+                for (int mt = 0; mt < kMt; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[mt][nt][e] += s2[mt][nt][e];
             }
             __syncwarp();
             if (!timed_out) issue(x + NH);  // the K slot is free again
@@ -506,6 +541,7 @@ __global__ void __maxnreg__(224)
                 v += __shfl_xor_sync(0xffffffffu, v, 16);
                 lrun[nt][j] = v;
             }
+        const int unit = wk.b * a.Hkv + wk.g;
         if (whole) {
             float* ob = a.out + ((long long)wk.b * a.Hq + wk.g * G) * D;
 #pragma unroll
@@ -522,8 +558,28 @@ __global__ void __maxnreg__(224)
                         }
                     }
                 }
+        } else if (cta_merge) {
+            if constexpr (kCtaMerge) {
+                const long long p0 = wk.start + a.unit_cost;  // the unit's pages: [p0, p0 + pb)
+                const int inside = p0 >= cta_s && p0 + wk.pb <= cta_e;
+                if (!nx.done) {  // the share's first piece; later units follow
+                    first_unit = unit;
+                    first_inside = inside;
+#pragma unroll
+                    for (int dt = 0; dt < kKs; ++dt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) of[dt][e] = o[dt][0][e];
+                    mf[0] = mrun[0][0];
+                    mf[1] = mrun[0][1];
+                    lf[0] = lrun[0][0];
+                    lf[1] = lrun[0][1];
+                } else {
+                    last_unit = unit;
+                    last_inside = inside;
+                }
+            }
         } else {
-            const long long slot = part + (long long)wk.b * a.Hkv + wk.g;
+            const long long slot = part + unit;
             float* accp = a.ws_acc + slot * G * D;
             float* ml = a.ws_ml + slot * G * 2;
 #pragma unroll
@@ -541,18 +597,136 @@ __global__ void __maxnreg__(224)
                     }
                 }
         }
+        if (nx.done) break;  // o / mrun / lrun keep the last piece
         wk = nx;
     }
     // A wait that gave up may leave copies in flight: wait (bounded) for them.
     if (timed_out && lane == 0)
         for (int s = 0; s < NH; ++s) mbar_wait(&my_full[s], ((x + s) / NH) & 1, 1024);
+    __syncwarp();
+    if (kCtaMerge && cta_merge) {
+        // Stage the non-whole pieces in this warp's own ring (its copies are
+        // all consumed): piece k is [G][D + 4] accumulators (the pad puts the
+        // 8 x 4 lanes of one store in 32 distinct banks) then [G] (m, l) pairs.
+        constexpr int kRow = D + 4;
+        const int pstride = (G * kRow + 2 * G + 3) & ~3;  // pieces stay 16-byte aligned
+        auto stage = [&](int k, const float (&src)[kKs][4], const float (&m)[2], const float (&l)[2]) {
+            float* pc = reinterpret_cast<float*>(my_tiles) + k * pstride;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int h = 2 * t4 + j;
+                if (h < G) {
+#pragma unroll
+                    for (int dt = 0; dt < kKs; ++dt) {
+                        pc[h * kRow + 16 * dt + g4] = src[dt][j];
+                        pc[h * kRow + 16 * dt + g4 + 8] = src[dt][2 + j];
+                    }
+                    if (g4 == 0) {
+                        pc[G * kRow + 2 * h] = m[j];
+                        pc[G * kRow + 2 * h + 1] = l[j];
+                    }
+                }
+            }
+        };
+        if (first_unit >= 0) stage(0, of, mf, lf);
+        if (last_unit >= 0) {
+            float ol[kKs][4], ml_[2] = {mrun[0][0], mrun[0][1]}, ll[2] = {lrun[0][0], lrun[0][1]};
+#pragma unroll
+            for (int dt = 0; dt < kKs; ++dt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ol[dt][e] = o[dt][0][e];
+            stage(1, ol, ml_, ll);
+        }
+        if (lane == 0) {
+            s_unit[warp][0] = first_unit;
+            s_inside[warp][0] = first_inside;
+            s_unit[warp][1] = last_unit;
+            s_inside[warp][1] = last_inside;
+        }
+        __syncthreads();
+        // Merge, unit by unit in warp order, the pieces that warps of this CTA
+        // share; a unit whose pages all lie in this CTA's share is finished
+        // here, the others leave one piece for the combine (slot CTA + unit).
+        // Every warp reads the 16 entry descriptors (lane f and f + 16 hold
+        // entry f) and finds, with ballots, where each unit's entries start and
+        // which entries hold it.  The code stays short: it runs once per CTA
+        // and launch, so its instructions are fetched cold.
+        const int f = lane & (2 * kCW - 1);
+        const int su = s_unit[f >> 1][f & 1];
+        const uint32_t vmask = __ballot_sync(0xffffffffu, su >= 0) & 0xffffu;
+        const uint32_t lower = vmask & ((1u << f) - 1u);
+        const int pu = __shfl_sync(0xffffffffu, su, lower ? 31 - __clz(lower) : 0);
+        const uint32_t starts = __ballot_sync(0xffffffffu, su >= 0 && (lower == 0 || pu != su)) & 0xffffu;
+        auto piece = [&](int ff) {
+            return reinterpret_cast<const float*>(base + size_t(ff >> 1) * NH * kTile) + (ff & 1) * pstride;
+        };
+        for (uint32_t sm = starts; sm; sm &= sm - 1) {
+            const int e = __ffs(sm) - 1;
+            const int u = __shfl_sync(0xffffffffu, su, e);
+            const uint32_t emask = __ballot_sync(0xffffffffu, su == u) & 0xffffu;
+            const bool inside = s_inside[e >> 1][e & 1] != 0;
+            const int ub = u / a.Hkv, ug = u % a.Hkv;
+            // Weights: warp w takes heads 2w and 2w + 1, one lane per entry;
+            // maxima and denominators by fixed 16-lane shuffle trees.
+            if (2 * warp < G) {
+                const int h = 2 * warp + (lane >> 4);
+                const bool mine = h < G && ((emask >> f) & 1u);
+                const float mm = mine ? piece(f)[G * kRow + 2 * h] : -INFINITY;
+                const float ll = mine ? piece(f)[G * kRow + 2 * h + 1] : 0.f;
+                float M = mm;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                const float w = mm != -INFINITY ? ex2(mm - M) : 0.f;
+                float den = w * ll;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+                if (h < G) {
+                    s_w[h][f] = w;
+                    if (f == 0) {
+                        s_md[h][0] = M;
+                        s_md[h][1] = den;
+                    }
+                }
+            }
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < G * D / 4; idx += kThreadsV1) {
+                const int h = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
+                float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+                uint32_t m = emask;
+                while (m) {  // two entries a step, in ascending order
+                    const int f0 = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int f1 = m ? __ffs(m) - 1 : f0;
+                    const float w0 = s_w[h][f0], w1 = m ? s_w[h][f1] : 0.f;
+                    const float4 v0 = *reinterpret_cast<const float4*>(piece(f0) + h * kRow + d4);
+                    const float4 v1 = *reinterpret_cast<const float4*>(piece(f1) + h * kRow + d4);
+                    if (m) m &= m - 1;
+                    num.x = fmaf(w1, v1.x, fmaf(w0, v0.x, num.x));
+                    num.y = fmaf(w1, v1.y, fmaf(w0, v0.y, num.y));
+                    num.z = fmaf(w1, v1.z, fmaf(w0, v0.z, num.z));
+                    num.w = fmaf(w1, v1.w, fmaf(w0, v0.w, num.w));
+                }
+                const float M = s_md[h][0], den = s_md[h][1];
+                if (inside) {
+                    const float inv = den > 0.f ? 1.f / den : 0.f;
+                    *reinterpret_cast<float4*>(a.out + ((long long)ub * a.Hq + ug * G + h) * D + d4) =
+                        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+                } else {
+                    const long long slot = (long long)blockIdx.x + u;
+                    *reinterpret_cast<float4*>(a.ws_acc + (slot * G + h) * D + d4) = num;
+                    if (d4 == 0) *reinterpret_cast<float2*>(a.ws_ml + (slot * G + h) * 2) = make_float2(M, den);
+                }
+            }
+            __syncthreads();  // s_w / s_md are reused by the next unit
+        }
+    }
 }
 
 // Merges the pieces of units that span several parts: one CTA per (sequence,
 // q head), one thread per output dim.  The CTA locates its pieces from the
 // lengths alone (a lane-parallel prefix over the sequences) before it waits
 // for the partial kernel through programmatic dependent launch; after the
-// wait, the (m, l) pairs of up to 32 pieces (one per lane) and their
+// wait, the (m, l) pairs of up to 28 pieces (one per lane) and their
 // accumulators (one per thread and piece) are loaded together, so a merge
 // costs about one L2 round trip.  Maxima and denominators are reduced by
 // fixed shuffle trees and the accumulators are summed in ascending part
@@ -561,7 +735,7 @@ __global__ void __maxnreg__(224)
 // runs fit beside its 256 x 224-register CTA.
 template <int D>
 __global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int P) {
-    constexpr int kBatch = 32;  // pieces loaded together
+    constexpr int kBatch = 28;  // pieces loaded together
     const int lane = threadIdx.x & 31, d = threadIdx.x;
     const int item = blockIdx.x;  // b * Hq + h
     const int b = item / a.Hq, h = item % a.Hq, g = h / a.G, r = h % a.G;
@@ -577,7 +751,9 @@ __global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int 
     T = warp_sum_ll(T);
     pre = warp_sum_ll(pre);
     const int pb = seq_pages(a.context_lens, b, P, a.max_len);
-    const long long n = parts_in_use(T > 0 ? T : 1, a);
+    const long long nc = ctas_in_use(T > 0 ? T : 1, a.n_ctas);
+    const bool cta = a.cta_pieces && T <= (long long)kCtaMergeMaxShare * nc;  // as the partial kernel
+    const long long n = cta ? nc : nc * kCW;  // parts of the piece partition
     long long c0 = 0;
     int np = 0;
     if (pb > 0) {  // the unit's pages sit at cost positions [p0, p0 + pb)
@@ -644,10 +820,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Page tiles per CTA: as many K/V page tiles as shared memory holds once a
-// combine CTA (static shared memory and the per-CTA reservation) has room.
+// combine CTA (the per-CTA reservation) and the kernel's static shared memory
+// have room.
 int tile_count(int D, int P) {
     const size_t tile = size_t(P) * D * 2;
-    const size_t room = size_t(kSmemLimit) - 1024 - v1_fixed_bytes() - 2048;
+    const size_t room = size_t(kSmemLimit) - 1024 - v1_fixed_bytes() - 2048 - 1024;
     const int n = int(room / tile);
     return n > kMaxTiles ? kMaxTiles : n;
 }
@@ -661,12 +838,13 @@ cudaError_t launch_partial(const CUtensorMap& k, const CUtensorMap& v, const V1P
                            cudaStream_t st) {
     auto kern = decode_v1<T, D, P, NT>;
     static bool configured = false;  // benign race: every caller sets the same value
+    const size_t dyn = smem_bytes(D, P, a.ntiles);  // a function of (D, P) alone
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<n_ctas, kThreadsV1, smem_bytes(D, P, a.ntiles), st>>>(k, v, a);
+    kern<<<n_ctas, kThreadsV1, dyn, st>>>(k, v, a);
     return cudaGetLastError();
 }
 
@@ -771,7 +949,8 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.max_blocks = call.max_blocks;
     a.max_len = call.max_blocks * P;
     a.scale_log2 = call.scale_log2;
-    a.n_parts = call.n_ctas * kCW;
+    a.n_ctas = call.n_ctas;
+    a.cta_pieces = G <= 8;
     a.ntiles = tile_count(D, P);
     a.head_first = head_first;
     a.unit_cost = kUnitCost;
