@@ -248,17 +248,8 @@ __global__ void __maxnreg__(224)
 
     pdl_launch_dependents();
 
-    // ---- this CTA's share of the cost space, and this warp's part of it ---------
-    const long long cost = total_cost(a, P);
-    const long long n_cta = ctas_in_use(cost, gridDim.x);
-    if (blockIdx.x >= n_cta) return;  // the whole CTA, before any CTA barrier
-    const long long n = n_cta * kCW;
-    const long long part = (long long)blockIdx.x * kCW + warp;
-    const long long cta_s = (long long)blockIdx.x * cost / n_cta, cta_e = (blockIdx.x + 1) * cost / n_cta;
-    // Small calls (short shares, few pages a warp) merge the warps' pieces in
-    // the CTA, so the combine sees one piece per CTA; larger ones leave each
-    // warp's pieces to the combine.  Uniform over the grid.
-    const bool cta_merge = kCtaMerge && cost <= (long long)kCtaMergeMaxShare * n_cta;
+    // ---- set-up that touches no global memory: it may overlap the kernel
+    // before this one (programmatic dependent launch) ----------------------------
     const int NH = min(a.ntiles / kCW, kMaxRing);
     uint8_t* my_tiles = base + size_t(warp) * NH * kTile;  // [NH][kTile]
     int* my_page = reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile) + warp * NH;
@@ -279,6 +270,19 @@ __global__ void __maxnreg__(224)
         s_unit[warp][0] = s_unit[warp][1] = -1;
     }
     __syncwarp();
+    pdl_wait_primary();  // the previous kernel's writes are visible from here on
+
+    // ---- this CTA's share of the cost space, and this warp's part of it ---------
+    const long long cost = total_cost(a, P);
+    const long long n_cta = ctas_in_use(cost, gridDim.x);
+    if (blockIdx.x >= n_cta) return;  // the whole CTA, before any CTA barrier
+    const long long n = n_cta * kCW;
+    const long long part = (long long)blockIdx.x * kCW + warp;
+    const long long cta_s = (long long)blockIdx.x * cost / n_cta, cta_e = (blockIdx.x + 1) * cost / n_cta;
+    // Small calls (short shares, few pages a warp) merge the warps' pieces in
+    // the CTA, so the combine sees one piece per CTA; larger ones leave each
+    // warp's pieces to the combine.  Uniform over the grid.
+    const bool cta_merge = kCtaMerge && cost <= (long long)kCtaMergeMaxShare * n_cta;
     Walk wk = walk_start(a, P, part * cost / n, (part + 1) * cost / n);
 
     // ---- load side: issue half-stage x (page x/2 of the share; K, then V)
@@ -736,6 +740,7 @@ __global__ void __maxnreg__(224)
 template <int D>
 __global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int P) {
     constexpr int kBatch = 28;  // pieces loaded together
+    pdl_launch_dependents();    // the next kernel may start its own set-up
     const int lane = threadIdx.x & 31, d = threadIdx.x;
     const int item = blockIdx.x;  // b * Hq + h
     const int b = item / a.Hq, h = item % a.Hq, g = h / a.G, r = h % a.G;
@@ -844,8 +849,20 @@ cudaError_t launch_partial(const CUtensorMap& k, const CUtensorMap& v, const V1P
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<n_ctas, kThreadsV1, dyn, st>>>(k, v, a);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the CTAs may start (and set up shared
+    // memory) while the previous kernel on the stream finishes; the kernel
+    // waits for it before its first global-memory access.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_ctas);
+    cfg.blockDim = dim3(kThreadsV1);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, k, v, a);
 }
 
 template <typename T, int D, int P>
