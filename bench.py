@@ -301,6 +301,21 @@ def decode_calls(rot, ops, torch, partial_only=False):
     return calls, launches, S
 
 
+def append_calls(rot, wl, ops, torch):
+    """pa_decode_append over the rotation: each step also writes its
+    sequences' new K/V rows (the same rows every replay) into its pages."""
+    from paged_kv_gqa_02_gb300 import inputs
+    k_new, v_new = inputs.make_append_rows(num_seqs=wl.num_seqs, num_kv_heads=wl.num_kv_heads,
+                                           head_dim=wl.head_dim, kv_dtype=wl.kv_dtype, seed=wl.seed)
+    kn, vn = ops.to_device(k_new, wl.kv_dtype), ops.to_device(v_new, wl.kv_dtype)
+    p = rot.params
+    nws = ops.decode_workspace_size(p)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    return [lambda s, i=i: ops.decode_append(p, rot.q[i], kn, vn, rot.k, rot.v, rot.bt[i], rot.cl, out=rot.out,
+                                             workspace=ws if nws else None, stream=s)
+            for i in range(rot.R)]
+
+
 def prefill_calls(rot, wl, ops, torch):
     p = rot.params
     calls = [lambda s, i=i: ops.prefill_chunk(p, rot.q[i], rot.cu, wl.total_q, max(wl.q_lens), rot.k,
@@ -398,6 +413,8 @@ def measure_workload(wl, ops, torch, K, W, world, l2, hbm_peak, flop_peak, clock
         part = pms / K
         dom_bytes = wl.kv_bytes() + wl.q_bytes()
         achieved = dom_bytes / (part * 1e-3) / 1e9
+        ams, _, _ = time_graph(torch, append_calls(rot, wl, ops, torch), K, W, world)
+        res["append_us_per_call"] = max_over_ranks(ams, world) / K * 1e3
         res.update(num_splits=S, launches_per_call=launches, ms_total=ms, us_per_call=per_call * 1e3,
                    gbs=wl.algorithmic_bytes() / (per_call * 1e-3) / 1e9,
                    frac_of_hbm=wl.algorithmic_bytes() / (per_call * 1e-3) / 1e9 / hbm_peak,
@@ -484,6 +501,7 @@ def run_ours(args):
                          f"sets of one {main['pool_pages']}-page pool (>= 3x the {l2 // 2**20} MiB L2)",
                    "timing": "CUDA graph replays, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
+        "decode_append_us_per_call": round(main["append_us_per_call"], 3) if "append_us_per_call" in main else None,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": None if e2e_ms is None else {

@@ -144,6 +144,32 @@ pa_status pa_decode(const pa_params *p, const void *q, const void *k_cache,
                     const int32_t *context_lens, float *out, void *workspace,
                     size_t workspace_bytes, uint32_t *dev_status, pa_stream_t stream);
 
+/* Decode with the new token's K/V appended in the same pass.  The pages
+ * scatter each new token's K and V into the paged pool before attention on
+ * the same stream (crucible paged attention results, the layer walk-through;
+ * crucible README, "Layout, and why it was nearly free": decode's K/V write
+ * goes through the page table).  For each sequence b with a valid length L_b
+ * (which counts the new token) and a valid page
+ * pg = block_tables[b][(L_b - 1) / page_size], rows k_new[b][g][:] and
+ * v_new[b][g][:] of every kv head g are written to slot (L_b - 1) % page_size
+ * of page pg of k_cache / v_cache; then out is pa_decode's over keys
+ * [0, L_b), the new token included.  Whatever the slot held before is
+ * neither read nor used.
+ *   k_new, v_new: [B][Hkv][D] in kv_dtype, contiguous, 16-byte aligned,
+ *                 device memory owned by the caller.
+ *   k_cache, v_cache: written at those slots only (caller-owned).
+ * Other arguments, the workspace, asynchrony and errors are as pa_decode's.
+ * With 16-bit K/V and automatic splits the write happens inside the
+ * attention kernel: the warp that copies a sequence's last page into shared
+ * memory replaces the row there and stores it to the cache.  Otherwise a
+ * scatter kernel writes the rows before the attention.  The slot must not
+ * be shared with another sequence of the same call. */
+pa_status pa_decode_append(const pa_params *p, const void *q, const void *k_new,
+                           const void *v_new, void *k_cache, void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           float *out, void *workspace, size_t workspace_bytes,
+                           uint32_t *dev_status, pa_stream_t stream);
+
 /* The partial step on its own.  For each sequence b, q head h and split i
  * in [0, num_splits) (num_splits from pa_decode_plan) it writes, with
  * idx = (b*Hq + h)*num_splits + i:

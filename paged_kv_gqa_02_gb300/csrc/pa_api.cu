@@ -226,10 +226,12 @@ PA_EXPORT pa_status pa_combine(const pa_params* p, const float* partial_ml,
                                              p->num_q_heads, num_splits, p->head_dim, stream));
 }
 
-PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_cache,
-                              const void* v_cache, const int32_t* block_tables,
-                              const int32_t* context_lens, float* out, void* workspace,
-                              size_t workspace_bytes, uint32_t* dev_status, pa_stream_t stream) {
+namespace {
+// pa_decode, with the new token's K/V appended first when k_new is set.
+pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, const void* v_new,
+                      const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                      const int32_t* context_lens, float* out, void* workspace, size_t workspace_bytes,
+                      uint32_t* dev_status, pa_stream_t stream) {
     Resolved r;
     pa_status st = check_params(p, &r);
     if (st != PA_OK) return st;
@@ -264,7 +266,17 @@ PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_c
         c.head_stride = r.head_stride;
         c.scale_log2 = p->scale * pa::kLog2e;
         c.phases = p->decode_phases ? p->decode_phases : 3;
+        c.k_new = k_new;  // fused: the partial kernel writes and attends the new rows
+        c.v_new = v_new;
         return cuda_status(pa::launch_decode_v1(c, stream));
+    }
+    if (k_new && (!p->decode_phases || (p->decode_phases & 1))) {
+        cudaError_t e = pa::launch_append_kv(k_new, v_new, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                                             block_tables, context_lens, p->num_seqs, p->num_kv_heads,
+                                             p->head_dim, p->page_size, p->kv_dtype == PA_F32 ? 4 : 2,
+                                             p->num_pages, p->max_blocks_per_seq, r.page_stride,
+                                             r.token_stride, r.head_stride, stream);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     const int phases = p->decode_phases ? p->decode_phases : 3;
     int S, tok;
@@ -291,6 +303,26 @@ PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_c
     if (!(phases & 2)) return PA_OK;
     return cuda_status(pa::launch_combine_v0(a.partial_ml, a.partial_acc, out, p->num_seqs,
                                              p->num_q_heads, S, p->head_dim, stream));
+}
+}  // namespace
+
+PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_cache,
+                              const void* v_cache, const int32_t* block_tables,
+                              const int32_t* context_lens, float* out, void* workspace,
+                              size_t workspace_bytes, uint32_t* dev_status, pa_stream_t stream) {
+    return decode_impl(p, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, out,
+                       workspace, workspace_bytes, dev_status, stream);
+}
+
+PA_EXPORT pa_status pa_decode_append(const pa_params* p, const void* q, const void* k_new,
+                                     const void* v_new, void* k_cache, void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     float* out, void* workspace, size_t workspace_bytes,
+                                     uint32_t* dev_status, pa_stream_t stream) {
+    if (!k_new || !v_new) return PA_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_ALIGN;
+    return decode_impl(p, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out,
+                       workspace, workspace_bytes, dev_status, stream);
 }
 
 PA_EXPORT size_t pa_prefill_workspace_size(const pa_params* p, int32_t total_q, int32_t max_q_len) {

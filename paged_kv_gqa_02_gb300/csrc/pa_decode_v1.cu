@@ -64,7 +64,36 @@ struct V1Params {
     float scale_log2;
     int32_t n_ctas, ntiles, head_first, unit_cost;
     int32_t cta_pieces;  // 1: the group fits one MMA column tile, so small calls merge per CTA
+    // KV append (nullptr: none): the new token of sequence b, kv head g is
+    // row L_b - 1 of the cache; it is written there and used in place of the
+    // row the page copy brought in
+    const void* k_new;  // [B][Hkv][D]
+    const void* v_new;
+    void* k_cache;
+    void* v_cache;
+    int64_t page_stride, token_stride, head_stride;  // elements
 };
+
+// Append: puts the new token's row (kv head g of sequence b) into row `row`
+// of a staged page tile (swizzled like the TMA copy) and into the cache.
+// Lanes 0 .. D/8 - 1 move one 16-byte chunk each.
+template <int D, int P>
+__device__ inline void append_row(uint8_t* tile, const void* src_all, void* cache, const V1Params& a, int b,
+                                  int g, int pg, int row) {
+    const int lane = threadIdx.x & 31;
+    if (lane < D / 8) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src_all) +
+                                                             ((long long)b * a.Hkv + g) * D) +
+                              lane);
+        const int c8 = lane & 7;
+        *reinterpret_cast<uint4*>(tile + (lane >> 3) * (P * 128) + row * 128 + ((c8 ^ (row & 7)) << 4)) = v;
+        uint16_t* dst = static_cast<uint16_t*>(cache) + (long long)pg * a.page_stride +
+                        (long long)row * a.token_stride + (long long)g * a.head_stride;
+        reinterpret_cast<uint4*>(dst)[lane] = v;
+    }
+    fence_proxy_async_smem();  // the tile is a TMA destination again later
+    __syncwarp();
+}
 
 // A warp's position in its share of the cost space.
 struct Walk {
@@ -403,6 +432,10 @@ __global__ void __maxnreg__(224)
                 if (lane == 0) flag(a.dev_status, PA_DEV_TIMEOUT);
             }
             const bool valid = ok && my_page[x % NH] >= 0;
+            const bool app = a.k_new != nullptr && i == wk.pb - 1;  // the unit's last page holds row L - 1
+            if (valid && app)
+                append_row<D, P>(my_tiles + size_t(x % NH) * kTile, a.k_new, a.k_cache, a, wk.b, wk.g,
+                                 my_page[x % NH], ntok - 1);
             if (valid) {
                 const uint32_t kb = smem_u32(my_tiles + size_t(x % NH) * kTile);
                 float s2[kMt][NT][4];  // one column tile: odd k-steps in a second accumulator (shorter chains)
@@ -504,6 +537,7 @@ __global__ void __maxnreg__(224)
             }
             if (valid && ok) {
                 uint8_t* vt = my_tiles + size_t(x % NH) * kTile;
+                if (app) append_row<D, P>(vt, a.v_new, a.v_cache, a, wk.b, wk.g, my_page[x % NH], ntok - 1);
                 if (ntok < P) {  // rows past the context hold arbitrary bits: zero them
                     for (int y = lane; y < (P - ntok) * kHalves * 8; y += 32) {
                         const int rowi = ntok + y / (kHalves * 8);
@@ -968,6 +1002,13 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.scale_log2 = call.scale_log2;
     a.n_ctas = call.n_ctas;
     a.cta_pieces = G <= 8;
+    a.k_new = call.k_new;
+    a.v_new = call.v_new;
+    a.k_cache = const_cast<void*>(call.k);
+    a.v_cache = const_cast<void*>(call.v);
+    a.page_stride = call.page_stride;
+    a.token_stride = call.token_stride;
+    a.head_stride = call.head_stride;
     a.ntiles = tile_count(D, P);
     a.head_first = head_first;
     a.unit_cost = kUnitCost;

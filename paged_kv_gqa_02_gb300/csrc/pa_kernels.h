@@ -30,11 +30,22 @@ struct DecodeV1Call {
     int64_t page_stride, token_stride, head_stride;
     float scale_log2;
     int phases;  // bit 0: partial kernel, bit 1: combine kernel
+    // KV append (both nullptr: none): [B][Hkv][D] rows written to row L_b - 1
+    // of the cache and attended in place of what it held
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
 };
 // Chunked prefill on the tensor cores (tcgen05): 16-bit Q/K/V, head_dim 128,
 // pages of 16 or 32 slots, G = Hq/Hkv <= 16, scale > 0.  Grid (Hkv * B, row tiles).
 bool prefill_tc_supported(pa_dtype dt, int D, int P, int G, float scale);
 cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st);
+
+// Writes the new token's K/V rows ([B][Hkv][D]) to row L_b - 1 of each
+// sequence's last page; sequences with an invalid length or page are skipped.
+cudaError_t launch_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens, int B, int Hkv,
+                             int D, int P, int elt_bytes, int num_pages, int max_blocks, int64_t page_stride,
+                             int64_t token_stride, int64_t head_stride, cudaStream_t st);
 
 size_t decode_v1_workspace_bytes(int B, int Hq, int Hkv, int D, int n_ctas);
 cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st);

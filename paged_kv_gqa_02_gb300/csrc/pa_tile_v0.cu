@@ -284,4 +284,43 @@ cudaError_t launch_combine_v0(const float* ml, const float* acc, float* out, int
     return cudaGetLastError();
 }
 
+namespace {
+// One CTA per sequence: the Hkv rows of its new token go to row L - 1 of
+// page block_tables[b][(L - 1) / P]; E is an unsigned type of the element size.
+template <typename E>
+__global__ void append_kv(const E* __restrict__ k_new, const E* __restrict__ v_new, E* k, E* v,
+                          const int32_t* __restrict__ bt, const int32_t* __restrict__ cl, int Hkv, int D, int P,
+                          int num_pages, int max_blocks, int64_t ps, int64_t ts, int64_t hs) {
+    const int b = blockIdx.x;
+    const int L = cl[b];
+    if (L < 1 || L > max_blocks * P) return;  // the attention flags it
+    const int pg = bt[(int64_t)b * max_blocks + (L - 1) / P];
+    if (pg < 0 || pg >= num_pages) return;
+    const int64_t row = (int64_t)pg * ps + (int64_t)((L - 1) % P) * ts;
+    for (int i = threadIdx.x; i < Hkv * D; i += blockDim.x) {
+        const int g = i / D, d = i - g * D;
+        k[row + g * hs + d] = k_new[((int64_t)b * Hkv + g) * D + d];
+        v[row + g * hs + d] = v_new[((int64_t)b * Hkv + g) * D + d];
+    }
+}
+}  // namespace
+
+cudaError_t launch_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens, int B, int Hkv,
+                             int D, int P, int elt_bytes, int num_pages, int max_blocks, int64_t page_stride,
+                             int64_t token_stride, int64_t head_stride, cudaStream_t st) {
+    const int threads = Hkv * D < 1024 ? Hkv * D : 1024;
+    if (elt_bytes == 4)
+        append_kv<uint32_t><<<B, threads, 0, st>>>(
+            static_cast<const uint32_t*>(k_new), static_cast<const uint32_t*>(v_new), static_cast<uint32_t*>(k_cache),
+            static_cast<uint32_t*>(v_cache), block_tables, context_lens, Hkv, D, P, num_pages, max_blocks,
+            page_stride, token_stride, head_stride);
+    else
+        append_kv<uint16_t><<<B, threads, 0, st>>>(
+            static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), static_cast<uint16_t*>(k_cache),
+            static_cast<uint16_t*>(v_cache), block_tables, context_lens, Hkv, D, P, num_pages, max_blocks,
+            page_stride, token_stride, head_stride);
+    return cudaGetLastError();
+}
+
 }  // namespace pa

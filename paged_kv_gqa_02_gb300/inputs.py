@@ -34,6 +34,8 @@ TID_Q = 1
 TID_K = 2
 TID_V = 3
 TID_TABLE = 4
+TID_K_NEW = 6   # new-token K rows of a decode-with-append call
+TID_V_NEW = 7
 
 DTYPES = ("f32", "f16", "bf16")
 
@@ -203,3 +205,12 @@ def make_paged_inputs(*, num_seqs: int, num_q_heads: int, num_kv_heads: int,
                 context_lens=np.asarray(context_lens, dtype=np.int32),
                 cu_q_lens=cu, num_pages=num_pages,
                 max_blocks_per_seq=max_blocks_per_seq)
+
+
+def make_append_rows(*, num_seqs: int, num_kv_heads: int, head_dim: int, kv_dtype: str,
+                     seed: int = DEFAULT_SEED):
+    """The new token's K and V rows of a decode-with-append call:
+    two [B][Hkv][D] arrays, N(0,1) rounded to the storage dtype."""
+    shape = (num_seqs, num_kv_heads, head_dim)
+    return (normal_tensor(seed, TID_K_NEW, shape, kv_dtype),
+            normal_tensor(seed, TID_V_NEW, shape, kv_dtype))

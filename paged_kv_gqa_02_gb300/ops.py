@@ -67,12 +67,13 @@ def load(path: str = LIB_PATH):
             L.pa_decode_workspace_size.restype = sz
             L.pa_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             L.pa_decode_partial.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
+            L.pa_decode_append.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             L.pa_combine.argtypes = [P, vp, vp, i32, vp, vp]
             L.pa_prefill_workspace_size.argtypes = [P, i32, i32]
             L.pa_prefill_workspace_size.restype = sz
             L.pa_prefill_chunk.argtypes = [P, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
-            for name in ("pa_decode_plan", "pa_decode", "pa_decode_partial", "pa_combine",
-                         "pa_prefill_chunk"):
+            for name in ("pa_decode_plan", "pa_decode", "pa_decode_append", "pa_decode_partial",
+                         "pa_combine", "pa_prefill_chunk"):
                 getattr(L, name).restype = ctypes.c_int
             L.pa_version.restype = i32
             _lib = L
@@ -157,6 +158,24 @@ def decode(p: Params, q, k_cache, v_cache, block_tables, context_lens, out=None,
     _check(load().pa_decode(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                             _ptr(block_tables), _ptr(context_lens), _ptr(out), _ptr(workspace),
                             nbytes, _ptr(dev_status), _stream(stream)), "pa_decode")
+    return out
+
+
+def decode_append(p: Params, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out=None,
+                  workspace=None, dev_status=None, stream=None):
+    """Decode with the new token's K/V ([B][Hkv][D]) written to row L-1 of each
+    sequence's last page first; k_cache / v_cache are updated in place."""
+    import torch
+    if out is None:
+        out = _empty_out(q, p)
+    if workspace is None:
+        n = decode_workspace_size(p)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device) if n else None
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pa_decode_append(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                   _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), _ptr(out),
+                                   _ptr(workspace), nbytes, _ptr(dev_status), _stream(stream)),
+           "pa_decode_append")
     return out
 
 
