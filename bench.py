@@ -316,6 +316,24 @@ def append_calls(rot, wl, ops, torch):
             for i in range(rot.R)]
 
 
+def rows_calls(rot, wl, ops, torch, T):
+    """pa_decode with T query rows per sequence (decode_q_rows) over the
+    rotation; lengths below T are raised to T (the pages hold those keys)."""
+    import copy
+    from paged_kv_gqa_02_gb300 import inputs
+    p = copy.copy(rot.params)
+    p.decode_q_rows = T
+    q = ops.to_device(inputs.normal_tensor(wl.seed, 8, (wl.num_seqs * T, wl.num_q_heads, wl.head_dim),
+                                           wl.q_dtype), wl.q_dtype)
+    cl = torch.clamp(rot.cl, min=T)
+    out = torch.empty((wl.num_seqs * T, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
+    nws = ops.decode_workspace_size(p)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    return [lambda s, i=i: ops.decode(p, q, rot.k, rot.v, rot.bt[i], cl, out=out,
+                                      workspace=ws if nws else None, stream=s)
+            for i in range(rot.R)]
+
+
 def prefill_calls(rot, wl, ops, torch):
     p = rot.params
     calls = [lambda s, i=i: ops.prefill_chunk(p, rot.q[i], rot.cu, wl.total_q, max(wl.q_lens), rot.k,
@@ -415,6 +433,9 @@ def measure_workload(wl, ops, torch, K, W, world, l2, hbm_peak, flop_peak, clock
         achieved = dom_bytes / (part * 1e-3) / 1e9
         ams, _, _ = time_graph(torch, append_calls(rot, wl, ops, torch), K, W, world)
         res["append_us_per_call"] = max_over_ranks(ams, world) / K * 1e3
+        for T in (2, 4):
+            tms, _, _ = time_graph(torch, rows_calls(rot, wl, ops, torch, T), K, W, world)
+            res[f"rows{T}_us_per_call"] = max_over_ranks(tms, world) / K * 1e3
         res.update(num_splits=S, launches_per_call=launches, ms_total=ms, us_per_call=per_call * 1e3,
                    gbs=wl.algorithmic_bytes() / (per_call * 1e-3) / 1e9,
                    frac_of_hbm=wl.algorithmic_bytes() / (per_call * 1e-3) / 1e9 / hbm_peak,
@@ -502,6 +523,8 @@ def run_ours(args):
                    "timing": "CUDA graph replays, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
         "decode_append_us_per_call": round(main["append_us_per_call"], 3) if "append_us_per_call" in main else None,
+        "decode_rows_us_per_call": {T: round(main[f"rows{T}_us_per_call"], 3) for T in (2, 4)
+                                    if f"rows{T}_us_per_call" in main},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": None if e2e_ms is None else {

@@ -99,6 +99,21 @@ typedef struct {
                                    only; 2 = combine step only (after a
                                    phase-1 call on the same workspace, to put
                                    other work between the two or time them)     */
+    int32_t decode_q_rows;      /* pa_decode: query rows per sequence, 0 or 1 =
+                                   one; up to 16 (speculative / multi-token
+                                   decode).  q and out are then [B][rows][Hq][D]
+                                   and row t of a sequence of length L sees keys
+                                   [0, L - rows + t] (causal among the rows, as
+                                   in chunked prefill; crucible README, "Prefill
+                                   scheduling").  L < rows is an invalid length.
+                                   16-bit K/V with automatic splits run on the
+                                   split-KV kernel with the rows as extra MMA
+                                   columns, in blocks of 16 / (Hq/Hkv) rows (one
+                                   K/V pass per block; decode_phases must then
+                                   be 0 when there are several blocks); fp32 K/V
+                                   take one CUDA-core pass per (sequence, kv
+                                   head), and num_splits must be 0.  Not with
+                                   pa_decode_partial or pa_decode_append.        */
 } pa_params;
 
 /* Fills *p with defaults: contiguous strides, PA_F32 out, automatic splits,

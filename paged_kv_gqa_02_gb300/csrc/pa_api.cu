@@ -16,6 +16,7 @@ using pa::AttnArgs;
 constexpr int kRefSms = 152;       // SM count behind the device-independent plan
 constexpr int kCtasPerSm = 4;      // split-plan target: CTAs per SM
 constexpr int kMinSplitPages = 2;  // smallest automatic split, in pages
+constexpr int kMaxDecodeRows = 16; // query rows per sequence in pa_decode
 
 int elt_bytes(pa_dtype d) { return d == PA_F32 ? 4 : 2; }
 
@@ -47,6 +48,8 @@ pa_status check_params(const pa_params* p, Resolved* r) {
     if (p->deterministic != 0 && p->deterministic != 1) return PA_ERR_SHAPE;
     if (p->num_splits < 0) return PA_ERR_SHAPE;
     if (p->decode_phases < 0 || p->decode_phases > 3) return PA_ERR_SHAPE;
+    if (p->decode_q_rows < 0 || p->decode_q_rows > kMaxDecodeRows) return PA_ERR_SHAPE;
+    if (p->decode_q_rows > p->max_context_len) return PA_ERR_SHAPE;
     const int64_t D = p->head_dim;
     r->head_stride = p->head_stride ? p->head_stride : D;
     r->token_stride = p->token_stride ? p->token_stride : p->num_kv_heads * r->head_stride;
@@ -106,7 +109,19 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // pa_decode takes the length-balanced v1 path for 16-bit K/V unless a split
 // count is requested; it needs one persistent CTA per (reference) SM.
+// Several query rows per sequence ride along as extra MMA columns (rows x
+// q heads of a kv head <= 16).
+int decode_rows(const pa_params* p) { return p->decode_q_rows > 1 ? p->decode_q_rows : 1; }
+
 bool use_v1(const pa_params* p) { return p->num_splits == 0 && p->kv_dtype != PA_F32; }
+
+// Rows per launch of the split-KV kernel: rows x q heads of a kv head are its
+// MMA columns, at most 16; more rows take several launches, one per block.
+int row_block(const pa_params* p) {
+    const int g = p->num_q_heads / p->num_kv_heads;
+    const int rb = 16 / g;
+    return decode_rows(p) < rb ? decode_rows(p) : rb;
+}
 
 int v1_ctas(const pa_params* p) { return p->deterministic ? kRefSms : device_sms(); }
 
@@ -183,8 +198,9 @@ PA_EXPORT size_t pa_decode_workspace_size(const pa_params* p) {
     Resolved r;
     if (check_params(p, &r) != PA_OK) return 0;
     if (use_v1(p))
-        return pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads, p->num_kv_heads,
-                                             p->head_dim, v1_ctas(p));
+        return pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads * row_block(p),
+                                             p->num_kv_heads, p->head_dim, v1_ctas(p));
+    if (decode_rows(p) > 1) return 0;  // one CUDA-core pass over every row, no splits
     int S, tok;
     plan(p, &S, &tok);
     if (S == 1) return 0;
@@ -204,6 +220,7 @@ PA_EXPORT pa_status pa_decode_partial(const pa_params* p, const void* q, const v
         return st;
     if (!partial_acc) return PA_ERR_NULL;
     if (!aligned16(partial_acc)) return PA_ERR_ALIGN;
+    if (decode_rows(p) > 1) return PA_ERR_UNSUPPORTED;
     int S, tok;
     plan(p, &S, &tok);
     if (num_splits != S) return PA_ERR_SHAPE;
@@ -236,9 +253,13 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
     pa_status st = check_params(p, &r);
     if (st != PA_OK) return st;
     if ((st = check_io(q, k_cache, v_cache, block_tables, context_lens, out)) != PA_OK) return st;
+    const int rows = decode_rows(p);
+    if (rows > 1 && k_new) return PA_ERR_UNSUPPORTED;  // the append takes one new token
     if (use_v1(p)) {
         const int n = v1_ctas(p);
-        const size_t need = pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads,
+        const int rb = row_block(p);
+        if (rows > rb && p->decode_phases != 0) return PA_ERR_UNSUPPORTED;  // one workspace per block
+        const size_t need = pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads * rb,
                                                           p->num_kv_heads, p->head_dim, n);
         if (!workspace) return PA_ERR_NULL;
         if (workspace_bytes < need) return PA_ERR_WORKSPACE;
@@ -266,9 +287,27 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         c.head_stride = r.head_stride;
         c.scale_log2 = p->scale * pa::kLog2e;
         c.phases = p->decode_phases ? p->decode_phases : 3;
+        c.rows = rows;
         c.k_new = k_new;  // fused: the partial kernel writes and attends the new rows
         c.v_new = v_new;
-        return cuda_status(pa::launch_decode_v1(c, stream));
+        for (int t0 = 0; t0 < rows; t0 += rb) {  // blocks of rows share the workspace in turn
+            c.row0 = t0;
+            c.row_count = rows - t0 < rb ? rows - t0 : rb;
+            const pa_status s = cuda_status(pa::launch_decode_v1(c, stream));
+            if (s != PA_OK) return s;
+        }
+        return PA_OK;
+    }
+    if (rows > 1) {  // every row of a sequence in one CUDA-core pass (no splits)
+        if (p->num_splits > 0) return PA_ERR_UNSUPPORTED;
+        if (p->decode_phases == 2) return PA_OK;
+        AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
+        a.out = out;
+        a.rows_per_seq = rows;
+        a.max_q_len = rows;
+        a.total_q = p->num_seqs * rows;
+        a.num_splits = 1;
+        return cuda_status(pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
     }
     if (k_new && (!p->decode_phases || (p->decode_phases & 1))) {
         cudaError_t e = pa::launch_append_kv(k_new, v_new, const_cast<void*>(k_cache), const_cast<void*>(v_cache),

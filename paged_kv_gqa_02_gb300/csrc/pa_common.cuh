@@ -34,6 +34,7 @@ struct AttnArgs {
     int32_t num_splits;   // S
     int32_t max_q_len;    // prefill: host bound on rows per sequence
     int32_t total_q;      // rows in q / out
+    int32_t rows_per_seq = 0;  // > 1 with cu_q_lens == nullptr: sequence b owns rows b*n .. b*n + n - 1
 };
 
 // ---- element conversions -------------------------------------------------

@@ -61,6 +61,9 @@ struct V1Params {
     float* ws_acc;  // [slot][G][D]
     uint32_t* dev_status;
     int32_t B, Hq, Hkv, G, num_pages, max_blocks, max_len;
+    int32_t T, t0, Gq;  // query rows per sequence, first row of this launch, q heads per kv
+                        // head.  G = rows * Gq columns per unit: column c is row
+                        // t0 + c / Gq, q head g * Gq + c % Gq
     float scale_log2;
     int32_t n_ctas, ntiles, head_first, unit_cost;
     int32_t cta_pieces;  // 1: the group fits one MMA column tile, so small calls merge per CTA
@@ -95,6 +98,22 @@ __device__ inline void append_row(uint8_t* tile, const void* src_all, void* cach
     __syncwarp();
 }
 
+__device__ inline int pages_of_len(int L, int P, int max_len, int T) {
+    return (L >= T && L >= 1 && L <= max_len) ? (L + P - 1) / P : 0;
+}
+
+// Pages of sequence b (0: invalid length, fewer keys than query rows).
+__device__ inline int seq_pages(const V1Params& a, int b, int P) {
+    return pages_of_len(__ldg(a.context_lens + b), P, a.max_len, a.T);
+}
+
+// Offset (elements) of column c of unit (b, g) in q and out: [B][T][Hq][D].
+template <int D>
+__device__ inline long long row_off(const V1Params& a, int b, int g, int c) {
+    const int tl = c / a.Gq;
+    return (((long long)b * a.T + a.t0 + tl) * a.Hq + (long long)g * a.Gq + (c - tl * a.Gq)) * D;
+}
+
 // A warp's position in its share of the cost space.
 struct Walk {
     long long start, s, e;  // cost position of the unit's first slot; share [s, e)
@@ -107,13 +126,6 @@ __host__ __device__ inline size_t v1_fixed_bytes() {
            + size_t(kMaxTiles) * 8;   // a full barrier per tile
 }
 
-__device__ inline int pages_of_len(int L, int P, int max_len) {
-    return (L >= 1 && L <= max_len) ? (L + P - 1) / P : 0;
-}
-
-__device__ inline int seq_pages(const int32_t* cl, int b, int P, int max_len) {
-    return pages_of_len(__ldg(cl + b), P, max_len);
-}
 
 __device__ inline long long warp_sum_ll(long long v) {
 #pragma unroll
@@ -134,7 +146,7 @@ __device__ inline long long warp_incl_scan_ll(long long v, int lane) {
 __device__ inline long long total_cost(const V1Params& a, int P) {
     long long tot = 0;
     for (int b = threadIdx.x & 31; b < a.B; b += 32) {
-        const int pb = seq_pages(a.context_lens, b, P, a.max_len);
+        const int pb = seq_pages(a, b, P);
         if (pb > 0) tot += (long long)a.Hkv * (pb + a.unit_cost);
     }
     return warp_sum_ll(tot);
@@ -148,7 +160,7 @@ __device__ inline Walk walk_start(const V1Params& a, int P, long long s, long lo
     long long basep = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int b = b0 + lane;
-        const int pb = b < a.B ? seq_pages(a.context_lens, b, P, a.max_len) : 0;
+        const int pb = b < a.B ? seq_pages(a, b, P) : 0;
         const long long c = pb > 0 ? (long long)a.Hkv * (pb + W) : 0;
         const long long incl = warp_incl_scan_ll(c, lane);
         const long long total = __shfl_sync(0xffffffffu, incl, 31);
@@ -181,7 +193,7 @@ __device__ inline void walk_next_unit(Walk& w, const V1Params& a, int P) {
         int pb = 0;
         do {
             ++w.b;
-        } while (w.b < a.B && (pb = seq_pages(a.context_lens, w.b, P, a.max_len)) == 0);
+        } while (w.b < a.B && (pb = seq_pages(a, w.b, P)) == 0);
         if (w.b >= a.B) {
             w.done = 1;
             return;
@@ -374,13 +386,13 @@ __global__ void __maxnreg__(224)
     uint32_t qb[NT][kKs][2], qn[NT][kKs][2];
     float o[kKs][NT][4];
     float sc[kMt][NT][4];
-    // B fragments of Q^T for unit (b, g): column n = q head nt*8 + g4 (0 past G)
+    // B fragments of Q^T for unit (b, g): column n = nt*8 + g4 (0 past G)
     auto load_q = [&](uint32_t (&dst)[NT][kKs][2], int b, int g) {
-        const T* qbase = static_cast<const T*>(a.q) + ((long long)b * a.Hq + g * G) * D;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int h = nt * 8 + g4;
-            const uint32_t* row = reinterpret_cast<const uint32_t*>(qbase + (h < G ? h : 0) * D);
+            const uint32_t* row =
+                reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.q) + row_off<D>(a, b, g, h < G ? h : 0));
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
                 dst[nt][ks][0] = h < G ? __ldg(row + 8 * ks + t4) : 0u;
@@ -389,6 +401,16 @@ __global__ void __maxnreg__(224)
         }
     };
     if (!wk.done) load_q(qn, wk.b, wk.g);
+    // Causal lag of the columns this lane holds (heads nt*8 + 2*t4 + j): row t
+    // of T sees keys [0, L - (T - 1 - t)).  Padding columns take no lag.
+    int lag[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c = nt * 8 + 2 * t4 + j;
+            lag[nt][j] = c < G ? a.T - 1 - (a.t0 + c / a.Gq) : 0;
+        }
     int x = 0;  // half-stage number
     // CTA merge (one q-head column tile): the share's first piece, when it is
     // not whole and other units follow, waits here; its last non-whole piece
@@ -423,7 +445,8 @@ __global__ void __maxnreg__(224)
             for (int nt = 0; nt < NT; ++nt) o[dt][nt][0] = o[dt][nt][1] = o[dt][nt][2] = o[dt][nt][3] = 0.f;
 
         for (int i = wk.pf; i < wk.pe; ++i) {
-            const int ntok = min(P, L - i * P);
+            const int rem = L - i * P;  // keys of this page and after it
+            const int ntok = min(P, rem);
             // ---- K tile: S^T = K Q^T, masked, online softmax
             bool ok = !timed_out;
             if (ok && !mbar_wait(&my_full[x % NH], (x / NH) & 1, kWaitLimit)) {
@@ -479,12 +502,12 @@ __global__ void __maxnreg__(224)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int tok = 16 * mt + g4 + ((e & 2) ? 8 : 0);
-                            const float v = tok < ntok ? sc[mt][nt][e] * a.scale_log2 : -INFINITY;
+                            const float v = tok < rem - lag[nt][e & 1] ? sc[mt][nt][e] * a.scale_log2 : -INFINITY;
                             sc[mt][nt][e] = v;
                             mx[nt][e & 1] = fmaxf(mx[nt][e & 1], v);
                         }
                 bool same = true;
-                float al[NT][2];
+                float al[NT][2], msf[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -494,7 +517,10 @@ __global__ void __maxnreg__(224)
                         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
                         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
                         const float mn = fmaxf(mrun[nt][j], v);
-                        al[nt][j] = ex2(mrun[nt][j] - mn);  // m = -inf -> 0
+                        // no visible key yet (a row of several whose keys end
+                        // before this page): offset 0 keeps every weight 0
+                        msf[nt][j] = mn == -INFINITY ? 0.f : mn;
+                        al[nt][j] = ex2(mrun[nt][j] - msf[nt][j]);  // m = -inf -> 0
                         same = same && al[nt][j] == 1.f;
                         mrun[nt][j] = mn;
                         lrun[nt][j] *= al[nt][j];
@@ -505,7 +531,7 @@ __global__ void __maxnreg__(224)
                     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            sc[mt][nt][e] = ex2(sc[mt][nt][e] - mrun[nt][e & 1]);
+                            sc[mt][nt][e] = ex2(sc[mt][nt][e] - msf[nt][e & 1]);
                             lrun[nt][e & 1] += sc[mt][nt][e];
                         }
 #pragma unroll
@@ -581,18 +607,18 @@ __global__ void __maxnreg__(224)
             }
         const int unit = wk.b * a.Hkv + wk.g;
         if (whole) {
-            float* ob = a.out + ((long long)wk.b * a.Hq + wk.g * G) * D;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int h = nt * 8 + 2 * t4 + j;
                     if (h < G) {
+                        float* ob = a.out + row_off<D>(a, wk.b, wk.g, h);
                         const float inv = lrun[nt][j] > 0.f ? 1.f / lrun[nt][j] : 0.f;
 #pragma unroll
                         for (int dt = 0; dt < kKs; ++dt) {
-                            ob[h * D + 16 * dt + g4] = o[dt][nt][j] * inv;
-                            ob[h * D + 16 * dt + g4 + 8] = o[dt][nt][2 + j] * inv;
+                            ob[16 * dt + g4] = o[dt][nt][j] * inv;
+                            ob[16 * dt + g4 + 8] = o[dt][nt][2 + j] * inv;
                         }
                     }
                 }
@@ -747,7 +773,7 @@ __global__ void __maxnreg__(224)
                 const float M = s_md[h][0], den = s_md[h][1];
                 if (inside) {
                     const float inv = den > 0.f ? 1.f / den : 0.f;
-                    *reinterpret_cast<float4*>(a.out + ((long long)ub * a.Hq + ug * G + h) * D + d4) =
+                    *reinterpret_cast<float4*>(a.out + row_off<D>(a, ub, ug, h) + d4) =
                         make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
                 } else {
                     const long long slot = (long long)blockIdx.x + u;
@@ -776,20 +802,22 @@ __global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int 
     constexpr int kBatch = 28;  // pieces loaded together
     pdl_launch_dependents();    // the next kernel may start its own set-up
     const int lane = threadIdx.x & 31, d = threadIdx.x;
-    const int item = blockIdx.x;  // b * Hq + h
-    const int b = item / a.Hq, h = item % a.Hq, g = h / a.G, r = h % a.G;
+    const int Tb = a.G / a.Gq;     // rows of this launch
+    const int item = blockIdx.x;  // (b * Tb + t) * Hq + q head
+    const int b = item / (Tb * a.Hq), rt = item % (Tb * a.Hq), t = rt / a.Hq, hq = rt % a.Hq;
+    const int g = hq / a.Gq, r = t * a.Gq + hq % a.Gq, h = hq;  // r: the unit's column
     const int unit = b * a.Hkv + g;
     const int W = a.unit_cost;
     long long T = 0, pre = 0;
     for (int x = lane; x < a.B; x += 32) {
-        const int pg = seq_pages(a.context_lens, x, P, a.max_len);
+        const int pg = seq_pages(a, x, P);
         const long long c = pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
         T += c;
         if (x < b) pre += c;
     }
     T = warp_sum_ll(T);
     pre = warp_sum_ll(pre);
-    const int pb = seq_pages(a.context_lens, b, P, a.max_len);
+    const int pb = seq_pages(a, b, P);
     const long long nc = ctas_in_use(T > 0 ? T : 1, a.n_ctas);
     const bool cta = a.cta_pieces && T <= (long long)kCtaMergeMaxShare * nc;  // as the partial kernel
     const long long n = cta ? nc : nc * kCW;  // parts of the piece partition
@@ -802,7 +830,7 @@ __global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int 
         np = c1 > c0 ? int(c1 - c0 + 1) : 0;  // 0: finished inside one part
     }
     pdl_wait_primary();  // the partial kernel's pieces are complete from here on
-    float* o = a.out + (long long)item * D + d;
+    float* o = a.out + (((long long)b * a.T + a.t0 + t) * a.Hq + hq) * D + d;
     if (pb == 0) {
         *o = 0.f;
         if (h == 0 && d == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
@@ -910,7 +938,7 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
     }
     if (!(phases & 2)) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(a.B) * unsigned(a.Hq));
+    cfg.gridDim = dim3(unsigned(a.B) * unsigned(a.G / a.Gq) * unsigned(a.Hq));
     cfg.blockDim = dim3(D);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -986,8 +1014,11 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.block_tables = call.block_tables;
     a.context_lens = call.context_lens;
     a.out = call.out;
-    const int G = call.Hq / call.Hkv;
-    const WsLayout wl = ws_layout(call.B, call.Hq, call.Hkv, D, call.n_ctas);
+    const int T = call.rows > 0 ? call.rows : 1;
+    const int nr = call.row_count > 0 ? call.row_count : T;  // rows of this launch
+    const int G = nr * (call.Hq / call.Hkv);  // columns per unit: rows x q heads of a kv head
+    if (G > 16 || call.row0 < 0 || call.row0 + nr > T) return cudaErrorInvalidValue;
+    const WsLayout wl = ws_layout(call.B, nr * call.Hq, call.Hkv, D, call.n_ctas);
     char* ws = static_cast<char*>(call.workspace);
     a.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
     a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
@@ -996,6 +1027,9 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.Hq = call.Hq;
     a.Hkv = call.Hkv;
     a.G = G;
+    a.T = T;
+    a.t0 = call.row0;
+    a.Gq = call.Hq / call.Hkv;
     a.num_pages = call.num_pages;
     a.max_blocks = call.max_blocks;
     a.max_len = call.max_blocks * P;

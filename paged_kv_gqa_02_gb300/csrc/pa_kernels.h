@@ -30,6 +30,9 @@ struct DecodeV1Call {
     int64_t page_stride, token_stride, head_stride;
     float scale_log2;
     int phases;  // bit 0: partial kernel, bit 1: combine kernel
+    int rows = 1;       // query rows per sequence (causal among them)
+    int row0 = 0;       // first row this launch handles
+    int row_count = 0;  // rows this launch handles (0: all); row_count x Hq/Hkv <= 16
     // KV append (both nullptr: none): [B][Hkv][D] rows written to row L_b - 1
     // of the cache and attended in place of what it held
     const void* k_new = nullptr;
@@ -47,6 +50,7 @@ cudaError_t launch_append_kv(const void* k_new, const void* v_new, void* k_cache
                              int D, int P, int elt_bytes, int num_pages, int max_blocks, int64_t page_stride,
                              int64_t token_stride, int64_t head_stride, cudaStream_t st);
 
+// Hq counts q heads times query rows per sequence.
 size_t decode_v1_workspace_bytes(int B, int Hq, int Hkv, int D, int n_ctas);
 cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st);
 

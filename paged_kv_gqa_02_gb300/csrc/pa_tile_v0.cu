@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.z, g = blockIdx.y, tile = blockIdx.x;
     const int G = a.group, Hq = a.num_q_heads;
-    const bool decode = (a.cu_q_lens == nullptr);
+    const bool fixed_rows = a.cu_q_lens == nullptr && a.rows_per_seq > 1;  // multi-row decode
+    const bool decode = a.cu_q_lens == nullptr && !fixed_rows;
 
     // ---- rows of this tile and their causal ends --------------------------
     int L = a.context_lens[b];
@@ -57,6 +58,9 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     if (decode) {
         row0 = b;
         Tq = 1;
+    } else if (fixed_rows) {
+        row0 = b * a.rows_per_seq;
+        Tq = a.rows_per_seq;
     } else {
         row0 = a.cu_q_lens[b];
         Tq = a.cu_q_lens[b + 1] - row0;
