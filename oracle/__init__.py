@@ -43,7 +43,7 @@ class Problem(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
-                ("max_blocks_per_seq", ctypes.c_int32), ("pad0", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("page_stride", ctypes.c_int64), ("token_stride", ctypes.c_int64),
                 ("head_stride", ctypes.c_int64), ("scale", ctypes.c_double),
                 ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
@@ -90,7 +90,7 @@ class _Bound:
     """Keeps the numpy arrays behind a Problem alive."""
 
     def __init__(self, inp, *, num_q_heads, num_kv_heads, head_dim, page_size, scale,
-                 q_dtype, kv_dtype, strides=None):
+                 q_dtype, kv_dtype, strides=None, window=0):
         q = np.ascontiguousarray(inp["q"])
         k = np.ascontiguousarray(inp["k_cache"])
         v = np.ascontiguousarray(inp["v_cache"])
@@ -104,7 +104,7 @@ class _Bound:
         self.Hq, self.D = num_q_heads, head_dim
         self.p = Problem(num_seqs=len(cl), num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                          head_dim=head_dim, page_size=page_size, num_pages=int(inp["num_pages"]),
-                         max_blocks_per_seq=bt.shape[1], pad0=0,
+                         max_blocks_per_seq=bt.shape[1], window=int(window),
                          page_stride=strides[0], token_stride=strides[1], head_stride=strides[2],
                          scale=float(scale), q_dtype=DTYPE_CODE[q_dtype],
                          kv_dtype=DTYPE_CODE[kv_dtype], q=q.ctypes.data, cu_q_lens=cu.ctypes.data,

@@ -34,7 +34,7 @@ def gather_dense(pool: np.ndarray, table_row: np.ndarray, L: int, page_size: int
 
 
 def attention(q, k_pool, v_pool, block_tables, context_lens, cu_q_lens,
-              num_q_heads, num_kv_heads, page_size, scale):
+              num_q_heads, num_kv_heads, page_size, scale, window=0):
     """q [total_q][Hq][D] (float64) -> out [total_q][Hq][D] (float64)."""
     group = num_q_heads // num_kv_heads
     out = np.zeros_like(q, dtype=np.float64)
@@ -50,6 +50,8 @@ def attention(q, k_pool, v_pool, block_tables, context_lens, cu_q_lens,
         S = np.einsum("thd,jhd->htj", Q, K) * scale     # [Hq][T][L]
         pos = (L - T) + np.arange(T)                    # absolute row positions
         visible = np.arange(L)[None, :] <= pos[:, None]  # [T][L]
+        if window > 0:                                  # only the last `window` keys of each row
+            visible &= np.arange(L)[None, :] > pos[:, None] - window
         S = np.where(visible[None], S, -np.inf)
         S = S - S.max(axis=2, keepdims=True)
         W = np.exp(S)

@@ -23,6 +23,10 @@
  *    whose context (history + these rows) is L_s keys; row r sits at
  *    absolute position start + r with start = L_s - T_s and attends keys
  *    0 ..= start + r.  Decode is T_s = 1, so it attends 0 .. L_s - 1.
+ *  - Sliding window (vllm.cpp PR #383 names a windowed instantiation of its
+ *    decode kernel without defining it; read here the plain way): with
+ *    window W > 0 a row whose causal end is e attends keys e - W + 1 ..= e
+ *    (those that exist), its last W keys.  W = 0 is no window.
  *  - Softmax and weighted sum: out = sum_j w_j v_j / sum_j w_j with
  *    w_j = exp(sigma_j - max_k sigma_k).  This is the exact result the
  *    online update of the crucible results (the online-softmax experiment)
@@ -49,7 +53,8 @@ enum { OR_OK = 0, OR_BAD_LEN = 1, OR_BAD_PAGE = 2, OR_BAD_ARG = 3 };
 
 typedef struct {
     int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, page_size;
-    int32_t num_pages, max_blocks_per_seq, pad0;
+    int32_t num_pages, max_blocks_per_seq;
+    int32_t window;              /* > 0: a row sees only its last `window` keys */
     int64_t page_stride, token_stride, head_stride; /* elements */
     double scale;
     int32_t q_dtype, kv_dtype;
@@ -136,11 +141,14 @@ static int attend_row(const or_problem *p, int64_t row, int h, double *out,
     const int start = L - T;
     int end = start + r;                                 /* inclusive causal end */
     if (g_mutation == 2) end = end - 1 < 0 ? 0 : end - 1; /* planted: off-by-one */
+    /* sliding window: keys end - window + 1 ..= end */
+    int lo = (p->window > 0 && end - p->window + 1 > 0) ? end - p->window + 1 : 0;
+    if (g_mutation == 8 && lo > 0) lo -= 1;               /* planted: window one key too wide */
     const int32_t *table = p->block_tables + (int64_t)s * p->max_blocks_per_seq;
     const int64_t qbase = (row * p->num_q_heads + h) * (int64_t)D;
 
     double mx = -INFINITY;
-    for (int j = 0; j <= end; ++j) {
+    for (int j = lo; j <= end; ++j) {
         int32_t page = table[j / P];
         int slot = j % P;
         if (g_mutation == 3) slot = (j + 1) % P;          /* planted: slot shift */
@@ -155,7 +163,7 @@ static int attend_row(const or_problem *p, int64_t row, int h, double *out,
     }
     double den = 0.0;
     for (int d = 0; d < D; ++d) out[d] = 0.0;
-    for (int j = 0; j <= end; ++j) {
+    for (int j = lo; j <= end; ++j) {
         int32_t page = table[j / P];
         int slot = j % P;
         if (g_mutation == 3) slot = (j + 1) % P;
@@ -170,7 +178,7 @@ static int attend_row(const or_problem *p, int64_t row, int h, double *out,
     }
     if (g_mutation == 7) den = den + 1.0;                /* planted: wrong normaliser */
     for (int d = 0; d < D; ++d) out[d] /= den;
-    *keys = (int64_t)end + 1;
+    *keys = (int64_t)(end - lo + 1);
     return OR_OK;
 }
 

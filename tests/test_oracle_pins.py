@@ -123,6 +123,51 @@ def pin_dense_agreement(cases=None):
     return ok
 
 
+def pin_window_one():
+    """Sliding window of 1: a row sees only its own position, so out is that
+    key's v exactly, for decode and prefill rows and every dtype."""
+    ok = True
+    for dt in ("f32", "f16", "bf16"):
+        inp, meta = problem(B=2, Hq=6, Hkv=3, D=16, P=4, lens=(9, 14), qlens=(1, 5), dt=dt, seed=41)
+        out = oracle.attention(inp, window=1, **meta)
+        for s in range(2):
+            L, r0, r1 = int(inp["context_lens"][s]), int(inp["cu_q_lens"][s]), int(inp["cu_q_lens"][s + 1])
+            for r in range(r0, r1):
+                end = L - (r1 - r0) + (r - r0)
+                for h in range(6):
+                    ok &= bool(np.array_equal(out[r, h], kv_vec(inp, meta, "v_cache", s, end, h // 2)))
+    return ok
+
+
+def pin_window_dense_agreement():
+    """Windowed attention against the dense brute force with the same window
+    mask, on random tiny shapes, decode and prefill rows."""
+    rng = np.random.default_rng(4321)
+    ok = True
+    for c in range(12):
+        P = int(rng.choice([4, 16]))
+        Hkv, G = int(rng.integers(1, 3)), int(rng.choice([1, 2, 4]))
+        B = int(rng.integers(1, 3))
+        lens = [int(x) for x in rng.integers(1, 60, size=B)]
+        qlens = [1 if c % 2 == 0 else int(rng.integers(1, L + 1)) for L in lens]
+        W = int(rng.integers(1, 40))
+        inp, meta = problem(B=B, Hq=G * Hkv, Hkv=Hkv, D=16, P=P, lens=lens, qlens=qlens,
+                            dt=("f32", "bf16")[c % 2], num_pages=sum((L + P - 1) // P for L in lens) + 3,
+                            seed=300 + c)
+        q, k, v = f64(inp, meta)
+        ref = dense.attention(q, k, v, inp["block_tables"], inp["context_lens"], inp["cu_q_lens"],
+                              meta["num_q_heads"], meta["num_kv_heads"], meta["page_size"], meta["scale"],
+                              window=W)
+        ok &= bool(np.abs(oracle.attention(inp, window=W, **meta) - ref).max() < 1e-12)
+    return ok
+
+
+def pin_window_wider_than_context():
+    """A window at least as long as the context changes nothing (bitwise)."""
+    inp, meta = problem(B=2, Hq=4, Hkv=2, D=16, P=8, lens=(37, 12), qlens=(1, 3), dt="f16", seed=43)
+    return bitwise_equal(oracle.attention(inp, window=37, **meta), oracle.attention(inp, **meta))
+
+
 def pin_page_boundaries():
     ok = True
     for P, lens in ((32, (1, 31, 32, 33, 63, 64, 65)), (16, (1, 15, 16, 17, 1023, 1024))):
@@ -158,7 +203,7 @@ def pin_outliers():
 
 PINS = [pin_length_one, pin_uniform_keys, pin_constant_v_per_group, pin_two_keys_closed_form,
         pin_dominant_key, pin_dense_agreement, pin_page_boundaries, pin_causal_positions,
-        pin_outliers]
+        pin_outliers, pin_window_one, pin_window_dense_agreement, pin_window_wider_than_context]
 
 
 def read_causal_golden():
@@ -186,9 +231,10 @@ def test_pin(pin):
 def test_planted_mistakes_are_caught():
     """Each deliberate mistake planted in the oracle (interleaved GQA mapping,
     off-by-one causal end, shifted slot, score sign, missing max shift,
-    reversed V index, wrong normaliser) fails at least one pin."""
+    reversed V index, wrong normaliser, window one key too wide) fails at
+    least one pin."""
     try:
-        for m in range(1, 8):
+        for m in range(1, 9):
             oracle.set_mutation(m)
             results = []
             for pin in PINS:
@@ -248,6 +294,21 @@ def test_future_poisoning_leaves_rows_unchanged():
         row_pois["v_cache"][pg, j % 8] = np.nan
     got = oracle.attention_one(row_pois, r, 1, **meta)
     assert bitwise_equal(got, base[r, 1])
+
+
+def test_keys_before_the_window_are_never_read():
+    """NaN in every key and value a row's window excludes leaves its output
+    unchanged (bitwise): the window is a read bound, not a mask."""
+    inp, meta = problem(B=1, Hq=4, Hkv=2, D=16, P=8, lens=(40,), qlens=(1,), dt="f32", seed=47)
+    W = 13
+    base = oracle.attention(inp, window=W, **meta)
+    k, v = inp["k_cache"].copy(), inp["v_cache"].copy()
+    for j in range(40 - W):
+        pg = inp["block_tables"][0][j // 8]
+        k[pg, j % 8] = np.nan
+        v[pg, j % 8] = np.nan
+    poisoned = dict(inp, k_cache=k, v_cache=v)
+    assert bitwise_equal(oracle.attention(poisoned, window=W, **meta), base)
 
 
 def test_prefill_row_equals_decode_at_that_length():
