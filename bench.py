@@ -334,6 +334,18 @@ def rows_calls(rot, wl, ops, torch, T):
             for i in range(rot.R)]
 
 
+def window_calls(rot, wl, ops, torch, W):
+    """pa_decode with a W-key sliding window over the rotation."""
+    import copy
+    p = copy.copy(rot.params)
+    p.sliding_window = W
+    nws = ops.decode_workspace_size(p)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    return [lambda s, i=i: ops.decode(p, rot.q[i], rot.k, rot.v, rot.bt[i], rot.cl, out=rot.out,
+                                      workspace=ws if nws else None, stream=s)
+            for i in range(rot.R)]
+
+
 def prefill_calls(rot, wl, ops, torch):
     p = rot.params
     calls = [lambda s, i=i: ops.prefill_chunk(p, rot.q[i], rot.cu, wl.total_q, max(wl.q_lens), rot.k,
@@ -436,6 +448,12 @@ def measure_workload(wl, ops, torch, K, W, world, l2, hbm_peak, flop_peak, clock
         for T in (2, 4):
             tms, _, _ = time_graph(torch, rows_calls(rot, wl, ops, torch, T), K, W, world)
             res[f"rows{T}_us_per_call"] = max_over_ranks(tms, world) / K * 1e3
+        if wl.kv_dtype != "f32":  # windows run on the split-KV kernel only
+            wms, _, _ = time_graph(torch, window_calls(rot, wl, ops, torch, 1024), K, W, world)
+            res["window1024_us_per_call"] = max_over_ranks(wms, world) / K * 1e3
+            wbytes = sum(min(L, 1024) for L in wl.context_lens) * 2 * wl.num_kv_heads * wl.head_dim * \
+                wl.elt(wl.kv_dtype) + wl.q_bytes() + wl.o_bytes()
+            res["window1024_gbs"] = wbytes / (res["window1024_us_per_call"] * 1e-6) / 1e9
         res.update(num_splits=S, launches_per_call=launches, ms_total=ms, us_per_call=per_call * 1e3,
                    gbs=wl.algorithmic_bytes() / (per_call * 1e-3) / 1e9,
                    frac_of_hbm=wl.algorithmic_bytes() / (per_call * 1e-3) / 1e9 / hbm_peak,
@@ -525,6 +543,8 @@ def run_ours(args):
         "decode_append_us_per_call": round(main["append_us_per_call"], 3) if "append_us_per_call" in main else None,
         "decode_rows_us_per_call": {T: round(main[f"rows{T}_us_per_call"], 3) for T in (2, 4)
                                     if f"rows{T}_us_per_call" in main},
+        "decode_window1024": {"us_per_call": round(main["window1024_us_per_call"], 3),
+                              "gbs": round(main["window1024_gbs"], 1)} if "window1024_us_per_call" in main else None,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": None if e2e_ms is None else {

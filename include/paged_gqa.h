@@ -114,6 +114,15 @@ typedef struct {
                                    take one CUDA-core pass per (sequence, kv
                                    head), and num_splits must be 0.  Not with
                                    pa_decode_partial or pa_decode_append.        */
+    int32_t sliding_window;     /* 0: none.  W > 0: a row whose causal end is
+                                   key e attends only keys e - W + 1 ..= e, its
+                                   last W keys (vllm.cpp PR #383 names a
+                                   windowed decode instantiation; this is the
+                                   plain reading).  Keys before every row's
+                                   window are never read.  pa_decode and
+                                   pa_decode_append with 16-bit K/V and
+                                   automatic splits only; otherwise
+                                   PA_ERR_UNSUPPORTED.                            */
 } pa_params;
 
 /* Fills *p with defaults: contiguous strides, PA_F32 out, automatic splits,

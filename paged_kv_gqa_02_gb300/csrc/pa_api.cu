@@ -50,6 +50,7 @@ pa_status check_params(const pa_params* p, Resolved* r) {
     if (p->decode_phases < 0 || p->decode_phases > 3) return PA_ERR_SHAPE;
     if (p->decode_q_rows < 0 || p->decode_q_rows > kMaxDecodeRows) return PA_ERR_SHAPE;
     if (p->decode_q_rows > p->max_context_len) return PA_ERR_SHAPE;
+    if (p->sliding_window < 0) return PA_ERR_SHAPE;
     const int64_t D = p->head_dim;
     r->head_stride = p->head_stride ? p->head_stride : D;
     r->token_stride = p->token_stride ? p->token_stride : p->num_kv_heads * r->head_stride;
@@ -220,7 +221,7 @@ PA_EXPORT pa_status pa_decode_partial(const pa_params* p, const void* q, const v
         return st;
     if (!partial_acc) return PA_ERR_NULL;
     if (!aligned16(partial_acc)) return PA_ERR_ALIGN;
-    if (decode_rows(p) > 1) return PA_ERR_UNSUPPORTED;
+    if (decode_rows(p) > 1 || p->sliding_window > 0) return PA_ERR_UNSUPPORTED;
     int S, tok;
     plan(p, &S, &tok);
     if (num_splits != S) return PA_ERR_SHAPE;
@@ -288,6 +289,7 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         c.scale_log2 = p->scale * pa::kLog2e;
         c.phases = p->decode_phases ? p->decode_phases : 3;
         c.rows = rows;
+        c.window = p->sliding_window;
         c.k_new = k_new;  // fused: the partial kernel writes and attends the new rows
         c.v_new = v_new;
         for (int t0 = 0; t0 < rows; t0 += rb) {  // blocks of rows share the workspace in turn
@@ -298,6 +300,7 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         }
         return PA_OK;
     }
+    if (p->sliding_window > 0) return PA_ERR_UNSUPPORTED;  // windows: split-KV kernel only
     if (rows > 1) {  // every row of a sequence in one CUDA-core pass (no splits)
         if (p->num_splits > 0) return PA_ERR_UNSUPPORTED;
         if (p->decode_phases == 2) return PA_OK;
@@ -386,6 +389,7 @@ PA_EXPORT pa_status pa_prefill_chunk(const pa_params* p, const void* q, const in
     if (!cu_q_lens) return PA_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u) return PA_ERR_ALIGN;
     if (total_q < 1 || max_q_len < 1 || max_q_len > p->max_context_len) return PA_ERR_SHAPE;
+    if (p->sliding_window > 0) return PA_ERR_UNSUPPORTED;  // decode only
     AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
     a.cu_q_lens = cu_q_lens;
     a.out = out;

@@ -61,6 +61,7 @@ struct V1Params {
     float* ws_acc;  // [slot][G][D]
     uint32_t* dev_status;
     int32_t B, Hq, Hkv, G, num_pages, max_blocks, max_len;
+    int32_t window;     // > 0: a row sees only its last `window` keys
     int32_t T, t0, Gq;  // query rows per sequence, first row of this launch, q heads per kv
                         // head.  G = rows * Gq columns per unit: column c is row
                         // t0 + c / Gq, q head g * Gq + c % Gq
@@ -102,9 +103,20 @@ __device__ inline int pages_of_len(int L, int P, int max_len, int T) {
     return (L >= T && L >= 1 && L <= max_len) ? (L + P - 1) / P : 0;
 }
 
-// Pages of sequence b (0: invalid length, fewer keys than query rows).
+// First page holding a key that a row of this launch sees (sliding window;
+// the launch's first row has the lowest window).
+__device__ inline int first_page(const V1Params& a, int L, int P) {
+    if (a.window <= 0) return 0;
+    const int lo = L - a.T + a.t0 - a.window + 1;
+    return lo > 0 ? lo / P : 0;
+}
+
+// Pages of sequence b that the unit reads (0: invalid length, fewer keys
+// than query rows): from first_page to the page of key L - 1.
 __device__ inline int seq_pages(const V1Params& a, int b, int P) {
-    return pages_of_len(__ldg(a.context_lens + b), P, a.max_len, a.T);
+    const int L = __ldg(a.context_lens + b);
+    const int n = pages_of_len(L, P, a.max_len, a.T);
+    return n > 0 ? n - first_page(a, L, P) : 0;
 }
 
 // Offset (elements) of column c of unit (b, g) in q and out: [B][T][Hq][D].
@@ -264,7 +276,9 @@ __device__ inline void window_fill(LoadWindow& lw, const V1Params& a, int P) {
     walk_advance(x, i, threadIdx.x & 31, a, P);
     lw.live = x.done ? 0 : 1;
     lw.g = x.g;
-    lw.page = lw.live ? __ldg(a.block_tables + (long long)x.b * a.max_blocks + i) : -1;
+    lw.page = lw.live ? __ldg(a.block_tables + (long long)x.b * a.max_blocks +
+                              first_page(a, __ldg(a.context_lens + x.b), P) + i)
+                      : -1;
 }
 
 // At most 224 registers a thread: 256 x 224 leaves room on the SM for one
@@ -421,6 +435,7 @@ __global__ void __maxnreg__(224)
 
     while (!wk.done) {
         const int L = __ldg(a.context_lens + wk.b);
+        const int fp = first_page(a, L, P);  // page i of the unit is page fp + i of the sequence
         const bool whole = (wk.pf == 0) && (wk.pe == wk.pb);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -445,7 +460,7 @@ __global__ void __maxnreg__(224)
             for (int nt = 0; nt < NT; ++nt) o[dt][nt][0] = o[dt][nt][1] = o[dt][nt][2] = o[dt][nt][3] = 0.f;
 
         for (int i = wk.pf; i < wk.pe; ++i) {
-            const int rem = L - i * P;  // keys of this page and after it
+            const int rem = L - (fp + i) * P;  // keys of this page and after it
             const int ntok = min(P, rem);
             // ---- K tile: S^T = K Q^T, masked, online softmax
             bool ok = !timed_out;
@@ -502,7 +517,9 @@ __global__ void __maxnreg__(224)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int tok = 16 * mt + g4 + ((e & 2) ? 8 : 0);
-                            const float v = tok < rem - lag[nt][e & 1] ? sc[mt][nt][e] * a.scale_log2 : -INFINITY;
+                            const int hi = rem - lag[nt][e & 1];  // keys [hi - window, hi) are visible
+                            const bool vis = tok < hi && (a.window <= 0 || tok >= hi - a.window);
+                            const float v = vis ? sc[mt][nt][e] * a.scale_log2 : -INFINITY;
                             sc[mt][nt][e] = v;
                             mx[nt][e & 1] = fmaxf(mx[nt][e & 1], v);
                         }
@@ -564,6 +581,18 @@ __global__ void __maxnreg__(224)
             if (valid && ok) {
                 uint8_t* vt = my_tiles + size_t(x % NH) * kTile;
                 if (app) append_row<D, P>(vt, a.v_new, a.v_cache, a, wk.b, wk.g, my_page[x % NH], ntok - 1);
+                // keys before every row's window in the first window page are
+                // never read: zero their V rows (0 * NaN would poison P V)
+                const int vlo = a.window > 0 && i == 0 ? L - a.T + a.t0 - a.window + 1 - fp * P : 0;
+                if (vlo > 0) {
+                    for (int y = lane; y < vlo * kHalves * 8; y += 32) {
+                        const int rowi = y / (kHalves * 8), rr = y % (kHalves * 8);
+                        *reinterpret_cast<uint4*>(vt + (rr >> 3) * (P * 128) + rowi * 128 + (rr & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
                 if (ntok < P) {  // rows past the context hold arbitrary bits: zero them
                     for (int y = lane; y < (P - ntok) * kHalves * 8; y += 32) {
                         const int rowi = ntok + y / (kHalves * 8);
@@ -1035,6 +1064,7 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.max_len = call.max_blocks * P;
     a.scale_log2 = call.scale_log2;
     a.n_ctas = call.n_ctas;
+    a.window = call.window;
     a.cta_pieces = G <= 8;
     a.k_new = call.k_new;
     a.v_new = call.v_new;

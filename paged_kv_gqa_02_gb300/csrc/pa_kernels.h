@@ -33,6 +33,7 @@ struct DecodeV1Call {
     int rows = 1;       // query rows per sequence (causal among them)
     int row0 = 0;       // first row this launch handles
     int row_count = 0;  // rows this launch handles (0: all); row_count x Hq/Hkv <= 16
+    int window = 0;     // > 0: each row sees only its last `window` keys
     // KV append (both nullptr: none): [B][Hkv][D] rows written to row L_b - 1
     // of the cache and attended in place of what it held
     const void* k_new = nullptr;

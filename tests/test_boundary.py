@@ -50,7 +50,36 @@ def test_params_struct_layout_matches_header(lib):
     p = ops.Params()
     lib.pa_params_init(ctypes.byref(p))
     assert (p.out_dtype, p.deterministic, p.num_splits, p.page_stride) == (ops.PA_F32, 1, 0, 0)
-    assert ctypes.sizeof(ops.Params) == 4 * 8 + 8 * 3 + 4 * 8
+    assert ctypes.sizeof(ops.Params) == header_layout()["sizeof"]
+
+
+def header_layout():
+    """sizeof(pa_params) and every field's offset, from a C compile of the header."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [f for f, _ in ops.Params._fields_]
+    src = "#include <stdio.h>\n#include <stddef.h>\n#include \"paged_gqa.h\"\nint main(void) {\n"
+    src += 'printf("sizeof %zu\\n", sizeof(pa_params));\n'
+    src += "".join(f'printf("{n} %zu\\n", offsetof(pa_params, {n}));\n' for n in names)
+    src += "return 0; }\n"
+    with tempfile.TemporaryDirectory() as d:
+        c, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        with open(c, "w") as f:
+            f.write(src)
+        subprocess.run([cc, "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    return {k: int(v) for k, v in (line.split() for line in out.splitlines())}
+
+
+def test_params_field_offsets_match_header():
+    """The ctypes binding's pa_params has the header's field offsets."""
+    layout = header_layout()
+    for name, _ in ops.Params._fields_:
+        assert getattr(ops.Params, name).offset == layout[name], name
 
 
 def test_status_strings(lib):
