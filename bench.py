@@ -495,7 +495,7 @@ def run_ours(args):
     clocks = sampler.summary(main.pop("t0"), main.pop("t1"))
     secondary = {}
     if not args.no_secondary:
-        for other in workloads.ALL:
+        for other in workloads.ALL + workloads.EXTRA:
             if other.name == wl.name:
                 continue
             k2 = 2000 if other.kind == "decode" else 20

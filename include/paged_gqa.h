@@ -39,7 +39,10 @@
  *    bit-identical results for identical inputs on every run.  With
  *    deterministic = 1 the split-KV partition is also independent of the
  *    device (a function of pa_params alone).
- *  - Supported: head_dim in {64, 128}; page_size in {16, 32};
+ *  - Supported: head_dim in {64, 128} everywhere, and 256 for pa_decode and
+ *    pa_decode_append with 16-bit K/V, automatic splits and at most 8 MMA
+ *    columns (query rows x Hq/Hkv) per block (PA_ERR_UNSUPPORTED otherwise);
+ *    page_size in {16, 32};
  *    num_q_heads % num_kv_heads == 0 with a ratio of at most 16;
  *    q_dtype == kv_dtype in {PA_F32, PA_F16, PA_BF16}; out_dtype = PA_F32;
  *    q, k_cache, v_cache and out 16-byte aligned; head_dim contiguous and

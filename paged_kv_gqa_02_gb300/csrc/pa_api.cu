@@ -37,7 +37,7 @@ pa_status check_params(const pa_params* p, Resolved* r) {
         p->kv_dtype > PA_BF16 || p->out_dtype < PA_F32 || p->out_dtype > PA_BF16)
         return PA_ERR_DTYPE;
     if (group > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
-    if (p->head_dim != 64 && p->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (p->page_size != 16 && p->page_size != 32) return PA_ERR_UNSUPPORTED;
     if (p->q_dtype != p->kv_dtype || p->out_dtype != PA_F32) return PA_ERR_UNSUPPORTED;
     if (p->num_pages < 1 || p->max_blocks_per_seq < 1 || p->max_context_len < 1)
@@ -114,13 +114,20 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // q heads of a kv head <= 16).
 int decode_rows(const pa_params* p) { return p->decode_q_rows > 1 ? p->decode_q_rows : 1; }
 
-bool use_v1(const pa_params* p) { return p->num_splits == 0 && p->kv_dtype != PA_F32; }
+bool use_v1(const pa_params* p) {
+    return p->num_splits == 0 && p->kv_dtype != PA_F32 &&
+           (p->head_dim != 256 || p->num_q_heads / p->num_kv_heads <= 8);
+}
+
+// head_dim 256 runs on the split-KV kernel only (16-bit K/V, automatic
+// splits, at most 8 MMA columns: rows x q heads of a kv head).
+bool d256_unsupported(const pa_params* p) { return p->head_dim == 256 && !use_v1(p); }
 
 // Rows per launch of the split-KV kernel: rows x q heads of a kv head are its
 // MMA columns, at most 16; more rows take several launches, one per block.
 int row_block(const pa_params* p) {
     const int g = p->num_q_heads / p->num_kv_heads;
-    const int rb = 16 / g;
+    const int rb = (p->head_dim == 256 ? 8 : 16) / g;
     return decode_rows(p) < rb ? decode_rows(p) : rb;
 }
 
@@ -198,6 +205,7 @@ PA_EXPORT pa_status pa_decode_plan(const pa_params* p, int32_t* num_splits, int3
 PA_EXPORT size_t pa_decode_workspace_size(const pa_params* p) {
     Resolved r;
     if (check_params(p, &r) != PA_OK) return 0;
+    if (d256_unsupported(p)) return 0;
     if (use_v1(p))
         return pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads * row_block(p),
                                              p->num_kv_heads, p->head_dim, v1_ctas(p));
@@ -221,7 +229,7 @@ PA_EXPORT pa_status pa_decode_partial(const pa_params* p, const void* q, const v
         return st;
     if (!partial_acc) return PA_ERR_NULL;
     if (!aligned16(partial_acc)) return PA_ERR_ALIGN;
-    if (decode_rows(p) > 1 || p->sliding_window > 0) return PA_ERR_UNSUPPORTED;
+    if (decode_rows(p) > 1 || p->sliding_window > 0 || p->head_dim == 256) return PA_ERR_UNSUPPORTED;
     int S, tok;
     plan(p, &S, &tok);
     if (num_splits != S) return PA_ERR_SHAPE;
@@ -239,6 +247,7 @@ PA_EXPORT pa_status pa_combine(const pa_params* p, const float* partial_ml,
     if (!p || !partial_ml || !partial_acc || !out) return PA_ERR_NULL;
     if (p->num_seqs < 1 || p->num_q_heads < 1 || num_splits < 1 || p->num_seqs > 65535)
         return PA_ERR_SHAPE;
+    if (p->head_dim == 256) return PA_ERR_UNSUPPORTED;
     if (p->head_dim != 64 && p->head_dim != 128) return PA_ERR_UNSUPPORTED;
     return cuda_status(pa::launch_combine_v0(partial_ml, partial_acc, out, p->num_seqs,
                                              p->num_q_heads, num_splits, p->head_dim, stream));
@@ -256,6 +265,7 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
     if ((st = check_io(q, k_cache, v_cache, block_tables, context_lens, out)) != PA_OK) return st;
     const int rows = decode_rows(p);
     if (rows > 1 && k_new) return PA_ERR_UNSUPPORTED;  // the append takes one new token
+    if (d256_unsupported(p)) return PA_ERR_UNSUPPORTED;
     if (use_v1(p)) {
         const int n = v1_ctas(p);
         const int rb = row_block(p);
@@ -389,7 +399,7 @@ PA_EXPORT pa_status pa_prefill_chunk(const pa_params* p, const void* q, const in
     if (!cu_q_lens) return PA_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u) return PA_ERR_ALIGN;
     if (total_q < 1 || max_q_len < 1 || max_q_len > p->max_context_len) return PA_ERR_SHAPE;
-    if (p->sliding_window > 0) return PA_ERR_UNSUPPORTED;  // decode only
+    if (p->sliding_window > 0 || p->head_dim == 256) return PA_ERR_UNSUPPORTED;  // decode only
     AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
     a.cu_q_lens = cu_q_lens;
     a.out = out;

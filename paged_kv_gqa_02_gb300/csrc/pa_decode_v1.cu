@@ -294,7 +294,7 @@ __global__ void __maxnreg__(224)
     constexpr int kKs = D / 16;         // k-steps of K Q^T; 16-dim row blocks of O^T
     // One column tile: warps of a CTA merge their pieces in shared memory.
     // Two: each warp's non-whole pieces go to the workspace.
-    constexpr bool kCtaMerge = NT == 1;
+    constexpr bool kCtaMerge = NT == 1 && D <= 128;  // D 256: per-warp pieces (registers)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -961,8 +961,13 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
                          int phases, cudaStream_t st) {
     if (phases & 1) {
         // one 8-wide column tile of q heads when the group fits, else two
-        cudaError_t e = a.G <= 8 ? launch_partial<T, D, P, 1>(k, v, a, n_ctas, st)
-                                 : launch_partial<T, D, P, 2>(k, v, a, n_ctas, st);
+        cudaError_t e;
+        if constexpr (D == 256) {  // one column tile only (accumulator registers)
+            e = a.G <= 8 ? launch_partial<T, D, P, 1>(k, v, a, n_ctas, st) : cudaErrorInvalidValue;
+        } else {
+            e = a.G <= 8 ? launch_partial<T, D, P, 1>(k, v, a, n_ctas, st)
+                         : launch_partial<T, D, P, 2>(k, v, a, n_ctas, st);
+        }
         if (e != cudaSuccess) return e;
     }
     if (!(phases & 2)) return cudaSuccess;
@@ -1065,7 +1070,7 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.scale_log2 = call.scale_log2;
     a.n_ctas = call.n_ctas;
     a.window = call.window;
-    a.cta_pieces = G <= 8;
+    a.cta_pieces = G <= 8 && D <= 128;  // as the partial kernel's kCtaMerge
     a.k_new = call.k_new;
     a.v_new = call.v_new;
     a.k_cache = const_cast<void*>(call.k);
@@ -1076,12 +1081,16 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.ntiles = tile_count(D, P);
     a.head_first = head_first;
     a.unit_cost = kUnitCost;
-    if (a.ntiles < 2 * kCW) return cudaErrorInvalidValue;
+    // at least one page tile per warp (head_dim 256 with 32-slot pages has
+    // one: its K and V copies then take turns in it)
+    if (a.ntiles < kCW) return cudaErrorInvalidValue;
     const bool bf = call.dtype == PA_BF16;
 #define PA_V1_CASE(DD, PP)                                                                        \
     if (D == DD && P == PP)                                                                       \
         return bf ? launch_typed<__nv_bfloat16, DD, PP>(mk, mv, a, call.n_ctas, call.phases, st) \
                   : launch_typed<__half, DD, PP>(mk, mv, a, call.n_ctas, call.phases, st);
+    PA_V1_CASE(256, 32)
+    PA_V1_CASE(256, 16)
     PA_V1_CASE(128, 32)
     PA_V1_CASE(128, 16)
     PA_V1_CASE(64, 32)

@@ -130,4 +130,10 @@ C5 = Workload(name="prefill_8x2048p512_64x8_d128", kind="prefill", num_seqs=8,
               shuffle=True, scale=1.0 / math.sqrt(128), tol=TOL_16)
 
 ALL = (C1, C2, C3, C4, C5)
-BY_NAME = {w.name: w for w in ALL}
+
+# Beyond the five: head_dim 256 decode (the pages' d256 variant) at the
+# 14B-shaped context, gqa 2, 16-slot pages.
+D256 = _decode("decode_16x8_d256_L3254", 1, 16, 8, 256, 16, "f16", [3254], 4096, True, tol=TOL_16)
+EXTRA = (D256,)
+
+BY_NAME = {w.name: w for w in ALL + EXTRA}
