@@ -11,6 +11,7 @@
 // fp32-KV decode path.  The split combine is at the end of this file.
 #include "pa_common.cuh"
 #include "pa_kernels.h"
+#include "pa_ptx.cuh"
 
 namespace pa {
 
@@ -51,6 +52,9 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     const int G = a.group, Hq = a.num_q_heads;
     const bool fixed_rows = a.cu_q_lens == nullptr && a.rows_per_seq > 1;  // multi-row decode
     const bool decode = a.cu_q_lens == nullptr && !fixed_rows;
+
+    pdl_launch_dependents();
+    pdl_wait_primary();  // the previous kernel's writes are visible from here on
 
     // ---- rows of this tile and their causal ends --------------------------
     int L = a.context_lens[b];
@@ -219,19 +223,38 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
 // Combine: one CTA per (q head, sequence), one thread per output dim.
 __global__ void combine_v0(const float* __restrict__ ml, const float* __restrict__ acc,
                            float* __restrict__ out, int Hq, int S, int D) {
-    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    // Batches of 16 splits: lane j holds split x0 + j's (m, l), every thread
+    // loads its dim of all 16 accumulators at once; batches are merged by
+    // rescaling in ascending split order (fixed shuffle trees, no atomics).
+    constexpr int kB = 16;
+    pdl_launch_dependents();
+    pdl_wait_primary();  // the partials are complete from here on
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31;
     const int64_t base = (int64_t(b) * Hq + h) * S;
-    float M = -INFINITY;
-    for (int i = 0; i < S; ++i) M = fmaxf(M, ml[(base + i) * 2]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-        for (int i = 0; i < S; ++i) {
-            const float m = ml[(base + i) * 2];
-            if (m == -INFINITY) continue;
-            const float w = ex2(m - M);
-            den = fmaf(w, ml[(base + i) * 2 + 1], den);
-            num = fmaf(w, acc[(base + i) * D + d], num);
+    float M = -INFINITY, num = 0.f, den = 0.f;
+    for (int x0 = 0; x0 < S; x0 += kB) {
+        const int cnt = min(kB, S - x0);
+        float mj = -INFINITY, lj = 0.f;
+        if (lane < cnt) {
+            const float2 v = *reinterpret_cast<const float2*>(ml + (base + x0 + lane) * 2);
+            mj = v.x;
+            lj = v.y;
         }
+        float av[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) av[j] = j < cnt ? acc[(base + x0 + j) * D + d] : 0.f;
+        const float Mn = fmaxf(M, warp_max(mj));
+        if (Mn == -INFINITY) continue;  // no key so far
+        const float sc = ex2(M - Mn);   // M = -inf -> 0
+        const float w = mj == -INFINITY ? 0.f : ex2(mj - Mn);
+        den = den * sc + warp_sum(w * lj);
+        num *= sc;
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            num = wj != 0.f ? fmaf(wj, av[j], num) : num;  // an empty split's acc is never written
+        }
+        M = Mn;
     }
     out[(int64_t(b) * Hq + h) * D + d] = den > 0.f ? num / den : 0.f;
 }
@@ -246,8 +269,19 @@ cudaError_t launch_one(const AttnArgs& a, dim3 grid, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    k<<<grid, kThreads, sm, st>>>(a);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the CTAs may start while the previous
+    // kernel finishes; the kernel waits for it before reading global memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 template <typename T, int R>
@@ -284,8 +318,16 @@ cudaError_t launch_prefill_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cuda
 
 cudaError_t launch_combine_v0(const float* ml, const float* acc, float* out, int B, int Hq,
                               int S, int D, cudaStream_t st) {
-    combine_v0<<<dim3(Hq, B), D, 0, st>>>(ml, acc, out, Hq, S, D);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(Hq, B);
+    cfg.blockDim = dim3(D);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_v0, ml, acc, out, Hq, S, D);
 }
 
 namespace {
