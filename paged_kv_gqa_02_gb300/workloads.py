@@ -134,6 +134,18 @@ ALL = (C1, C2, C3, C4, C5)
 # Beyond the five: head_dim 256 decode (the pages' d256 variant) at the
 # 14B-shaped context, gqa 2, 16-slot pages.
 D256 = _decode("decode_16x8_d256_L3254", 1, 16, 8, 256, 16, "f16", [3254], 4096, True, tol=TOL_16)
-EXTRA = (D256,)
+# Packed small-chunk prefill: crucible's "16x16" shape (16 fresh requests of
+# 16 rows, 12 q / 3 kv heads, D64, 16-token pages, f32; crucible paged
+# attention results, the shape table), and the same packing at 32 q / 8 kv
+# heads, D128, bf16 on the tensor cores.
+PACK_F32 = Workload(name="prefill_16x16_12x3_d64_f32", kind="prefill", num_seqs=16, num_q_heads=12,
+                    num_kv_heads=3, head_dim=64, page_size=16, q_dtype="f32", kv_dtype="f32",
+                    context_lens=(16,) * 16, q_lens=(16,) * 16, num_pages=4096, max_blocks_per_seq=1,
+                    shuffle=True, scale=1.0 / math.sqrt(64), tol=TOL_F32)
+PACK_BF16 = Workload(name="prefill_16x16_32x8_d128_bf16", kind="prefill", num_seqs=16, num_q_heads=32,
+                     num_kv_heads=8, head_dim=128, page_size=32, q_dtype="bf16", kv_dtype="bf16",
+                     context_lens=(16,) * 16, q_lens=(16,) * 16, num_pages=4096, max_blocks_per_seq=1,
+                     shuffle=True, scale=1.0 / math.sqrt(128), tol=TOL_16)
+EXTRA = (D256, PACK_F32, PACK_BF16)
 
 BY_NAME = {w.name: w for w in ALL + EXTRA}
