@@ -114,9 +114,11 @@ typedef struct {
                                    columns, in blocks of 16 / (Hq/Hkv) rows (one
                                    K/V pass per block; decode_phases must then
                                    be 0 when there are several blocks); fp32 K/V
-                                   take one CUDA-core pass per (sequence, kv
-                                   head), and num_splits must be 0.  Not with
-                                   pa_decode_partial or pa_decode_append.        */
+                                   take the CUDA-core pass over tiles of 4 rows
+                                   x the automatic key splits, then the combine
+                                   per (row, q head); num_splits must be 0.
+                                   Not with pa_decode_partial or
+                                   pa_decode_append.                             */
     int32_t sliding_window;     /* 0: none.  W > 0: a row whose causal end is
                                    key e attends only keys e - W + 1 ..= e, its
                                    last W keys (vllm.cpp PR #383 names a

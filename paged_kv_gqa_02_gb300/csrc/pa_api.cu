@@ -15,7 +15,7 @@ using pa::AttnArgs;
 
 constexpr int kRefSms = 152;       // SM count behind the device-independent plan
 constexpr int kCtasPerSm = 4;      // split-plan target: CTAs per SM
-constexpr int kMinSplitPages = 2;  // smallest automatic split, in pages
+constexpr int kMinSplitPages = 1;  // smallest automatic split, in pages
 constexpr int kMaxDecodeRows = 16; // query rows per sequence in pa_decode
 
 int elt_bytes(pa_dtype d) { return d == PA_F32 ? 4 : 2; }
@@ -131,10 +131,14 @@ int row_block(const pa_params* p) {
     return decode_rows(p) < rb ? decode_rows(p) : rb;
 }
 
+// The combine's grid holds one row of CTAs per (sequence, query row).
+bool rows_split_ok(const pa_params* p) { return int64_t(p->num_seqs) * decode_rows(p) <= 65535; }
+
 int v1_ctas(const pa_params* p) { return p->deterministic ? kRefSms : device_sms(); }
 
-size_t partial_bytes(const pa_params* p, int S, size_t* acc_off) {
-    const size_t n = size_t(p->num_seqs) * p->num_q_heads * S;
+// Split partials of every (row, q head): rows = query rows per sequence.
+size_t partial_bytes(const pa_params* p, int S, size_t* acc_off, int rows = 1) {
+    const size_t n = size_t(p->num_seqs) * rows * p->num_q_heads * S;
     *acc_off = align256(n * 2 * sizeof(float));
     return *acc_off + align256(n * p->head_dim * sizeof(float));
 }
@@ -209,12 +213,11 @@ PA_EXPORT size_t pa_decode_workspace_size(const pa_params* p) {
     if (use_v1(p))
         return pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads * row_block(p),
                                              p->num_kv_heads, p->head_dim, v1_ctas(p));
-    if (decode_rows(p) > 1) return 0;  // one CUDA-core pass over every row, no splits
     int S, tok;
     plan(p, &S, &tok);
-    if (S == 1) return 0;
+    if (S == 1 || !rows_split_ok(p)) return 0;
     size_t off;
-    return partial_bytes(p, S, &off);
+    return partial_bytes(p, S, &off, decode_rows(p));
 }
 
 PA_EXPORT pa_status pa_decode_partial(const pa_params* p, const void* q, const void* k_cache,
@@ -311,16 +314,37 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         return PA_OK;
     }
     if (p->sliding_window > 0) return PA_ERR_UNSUPPORTED;  // windows: split-KV kernel only
-    if (rows > 1) {  // every row of a sequence in one CUDA-core pass (no splits)
+    const int phases = p->decode_phases ? p->decode_phases : 3;
+    int S, tok;
+    plan(p, &S, &tok);
+    if (rows > 1) {  // CUDA-core pass over row tiles x key splits, then the combine per (row, head)
         if (p->num_splits > 0) return PA_ERR_UNSUPPORTED;
-        if (p->decode_phases == 2) return PA_OK;
+        if (!rows_split_ok(p)) S = 1;
         AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
-        a.out = out;
         a.rows_per_seq = rows;
         a.max_q_len = rows;
         a.total_q = p->num_seqs * rows;
-        a.num_splits = 1;
-        return cuda_status(pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
+        a.num_splits = S;
+        a.split_tokens = tok;
+        if (S == 1) {
+            a.out = out;
+            if (!(phases & 1)) return PA_OK;
+            return cuda_status(pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
+        }
+        size_t acc_off;
+        const size_t need = partial_bytes(p, S, &acc_off, rows);
+        if (!workspace) return PA_ERR_NULL;
+        if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_ALIGN;
+        a.partial_ml = static_cast<float*>(workspace);
+        a.partial_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_off);
+        if (phases & 1) {
+            cudaError_t e = pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream);
+            if (e != cudaSuccess) return PA_ERR_CUDA;
+        }
+        if (!(phases & 2)) return PA_OK;
+        return cuda_status(pa::launch_combine_v0(a.partial_ml, a.partial_acc, out, p->num_seqs * rows,
+                                                 p->num_q_heads, S, p->head_dim, stream));
     }
     if (k_new && (!p->decode_phases || (p->decode_phases & 1))) {
         cudaError_t e = pa::launch_append_kv(k_new, v_new, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
@@ -330,9 +354,6 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
                                              r.token_stride, r.head_stride, stream);
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
-    const int phases = p->decode_phases ? p->decode_phases : 3;
-    int S, tok;
-    plan(p, &S, &tok);
     AttnArgs a = base_args(p, r, q, k_cache, v_cache, block_tables, context_lens, dev_status);
     a.split_tokens = tok;
     a.num_splits = S;

@@ -48,10 +48,15 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     float* al_s = l_s + S::kDist;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.z, g = blockIdx.y, tile = blockIdx.x;
+    const int b = blockIdx.z, g = blockIdx.y;
     const int G = a.group, Hq = a.num_q_heads;
     const bool fixed_rows = a.cu_q_lens == nullptr && a.rows_per_seq > 1;  // multi-row decode
     const bool decode = a.cu_q_lens == nullptr && !fixed_rows;
+    // Split partials: x indexes the key split (one row), or row tile x split
+    // for several rows per sequence; a direct pass has one split.
+    const int Sn = a.out == nullptr ? a.num_splits : 1;
+    const int split = decode ? blockIdx.x : blockIdx.x % Sn;
+    const int tile = decode ? 0 : blockIdx.x / Sn;
 
     pdl_launch_dependents();
     pdl_wait_primary();  // the previous kernel's writes are visible from here on
@@ -72,11 +77,11 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     const bool bad = (Tq < 0) || (row0 < 0) || (L < Tq) || (L > a.max_blocks_per_seq * P) ||
                      (!decode && Tq > a.max_q_len);
     if (bad) {
-        if (tid == 0 && tile == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
+        if (tid == 0 && blockIdx.x == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
         L = 0;  // no key is read; the tile's rows are written as zeros
     }
     const int start = L - Tq;
-    const int r_first = decode ? 0 : tile * R;
+    const int r_first = tile * R;
     // rows of this tile that exist: below T (and the host bound), inside q/out
     int n_rows = 1;
     if (!decode) {
@@ -85,15 +90,40 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     }
     const int nd = R * G;
 
-    // key range [t0, t1)
-    int t0, t1;
-    if (decode) {
-        t0 = tile * a.split_tokens;
-        t1 = min(L, t0 + a.split_tokens);
-    } else {
-        t0 = 0;
-        t1 = (n_rows > 0 && !bad) ? start + r_first + n_rows : 0;
+    // key range [t0, t1): up to the tile's last causal end, cut to the split
+    int t0 = 0, t1 = decode ? L : ((n_rows > 0 && !bad) ? start + r_first + n_rows : 0);
+    if (a.out == nullptr) {
+        t0 = split * a.split_tokens;  // a whole number of pages
+        t1 = min(t1, t0 + a.split_tokens);
     }
+
+    const T* kbase = static_cast<const T*>(a.k) + int64_t(g) * a.head_stride;
+    const T* vbase = static_cast<const T*>(a.v) + int64_t(g) * a.head_stride;
+    const int32_t* table = a.block_tables + int64_t(b) * a.max_blocks_per_seq;
+
+    // Page rows of kv head g travel through registers: every 16-byte load of
+    // a page is issued before the first one is used, and the next page's
+    // loads are in flight while this page is computed.
+    constexpr int kLd = (P * kChunks + kThreads - 1) / kThreads;  // loads per thread, K and V each
+    uint4 kr[kLd], vr[kLd];
+    auto valid = [&](int32_t pg) { return pg >= 0 && pg < a.num_pages; };  // uniform across the CTA
+    auto fetch = [&](int32_t pg, int ps) {
+        const int n = min(P, t1 - ps);
+#pragma unroll
+        for (int u = 0; u < kLd; ++u) {
+            const int i = tid + u * kThreads;
+            if (i < n * kChunks) {
+                const int j = i / kChunks, c = i % kChunks;
+                const int64_t off = int64_t(pg) * a.page_stride + int64_t(j) * a.token_stride + c * kVec;
+                kr[u] = *reinterpret_cast<const uint4*>(kbase + off);
+                vr[u] = *reinterpret_cast<const uint4*>(vbase + off);
+            }
+        }
+    };
+    // The first table entry does not wait for the length: its index is known.
+    const int32_t first = t0 / P < a.max_blocks_per_seq ? table[t0 / P] : -1;
+    int32_t next = t0 < t1 ? first : -1;
+    if (t0 < t1 && valid(next)) fetch(next, t0);  // in flight while q is staged
 
     // ---- stage q (times scale*log2e) and reset the running state ----------
     for (int i = tid; i < nd * D; i += kThreads) {
@@ -115,30 +145,33 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     const int my_d = tid % D, my_grp = tid / D;
     __syncthreads();
 
-    const T* kbase = static_cast<const T*>(a.k) + int64_t(g) * a.head_stride;
-    const T* vbase = static_cast<const T*>(a.v) + int64_t(g) * a.head_stride;
-    const int32_t* table = a.block_tables + int64_t(b) * a.max_blocks_per_seq;
-
     for (int ps = t0; ps < t1; ps += P) {
         const int n = min(P, t1 - ps);
-        const int32_t page = table[ps / P];
-        if (page < 0 || page >= a.num_pages) {  // uniform across the CTA
+        const int32_t page = next;
+        if (valid(page)) {  // -- registers -> shared (fp32)
+#pragma unroll
+            for (int u = 0; u < kLd; ++u) {
+                const int i = tid + u * kThreads;
+                if (i < n * kChunks) {
+                    const int j = i / kChunks, c = i % kChunks;
+                    float f[kVec];
+                    vec_to_f32<T>(kr[u], f);
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) k_s[j * (D + 1) + c * kVec + e] = f[e];
+                    vec_to_f32<T>(vr[u], f);
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) v_s[j * D + c * kVec + e] = f[e];
+                }
+            }
+        }
+        next = ps + P < t1 ? table[(ps + P) / P] : -1;
+        if (!valid(page)) {
             if (tid == 0) flag(a.dev_status, PA_DEV_BAD_PAGE);
+            if (ps + P < t1 && valid(next)) fetch(next, ps + P);
             continue;
         }
-        // -- page rows of kv head g -> shared (fp32)
-        for (int i = tid; i < n * kChunks; i += kThreads) {
-            const int j = i / kChunks, c = i % kChunks;
-            const int64_t off = int64_t(page) * a.page_stride + int64_t(j) * a.token_stride + c * kVec;
-            float f[kVec];
-            vec_to_f32<T>(*reinterpret_cast<const uint4*>(kbase + off), f);
-#pragma unroll
-            for (int e = 0; e < kVec; ++e) k_s[j * (D + 1) + c * kVec + e] = f[e];
-            vec_to_f32<T>(*reinterpret_cast<const uint4*>(vbase + off), f);
-#pragma unroll
-            for (int e = 0; e < kVec; ++e) v_s[j * D + c * kVec + e] = f[e];
-        }
         __syncthreads();
+        if (ps + P < t1 && valid(next)) fetch(next, ps + P);
         // -- scores (base-2 units), masked per row's causal end
         for (int i = tid; i < nd * P; i += kThreads) {
             const int dist = i / P, j = i % P, r = dist / G;
@@ -190,17 +223,19 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     }
 
     // ---- outputs -------------------------------------------------------------
-    if (a.out == nullptr) {  // decode split partial
-        const int s = tile, Sn = a.num_splits;
+    if (a.out == nullptr) {  // split partial of each (row, q head): (m, l) and the unscaled sum
 #pragma unroll
         for (int k = 0; k < kPerThread; ++k) {
-            const int h = my_grp + k * S::kGroups;
-            if (h < G) {
-                const int64_t idx = (int64_t(b) * Hq + g * G + h) * Sn + s;
-                if (m_s[h] != -INFINITY) a.partial_acc[idx * D + my_d] = acc[k];
-                if (my_d == 0) {
-                    a.partial_ml[idx * 2] = m_s[h];
-                    a.partial_ml[idx * 2 + 1] = l_s[h];
+            const int dist = my_grp + k * S::kGroups;
+            if (dist < nd) {
+                const int r = dist / G, h = dist % G;
+                if (r < n_rows) {
+                    const int64_t idx = (int64_t(row0 + r_first + r) * Hq + g * G + h) * Sn + split;
+                    if (m_s[dist] != -INFINITY) a.partial_acc[idx * D + my_d] = acc[k];
+                    if (my_d == 0) {
+                        a.partial_ml[idx * 2] = m_s[dist];
+                        a.partial_ml[idx * 2 + 1] = l_s[dist];
+                    }
                 }
             }
         }
@@ -312,7 +347,9 @@ cudaError_t launch_decode_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cudaS
 
 cudaError_t launch_prefill_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st) {
     constexpr int R = 4;
-    dim3 grid((a.max_q_len + R - 1) / R, a.num_kv_heads, a.num_seqs);
+    const int splits = a.out == nullptr ? a.num_splits : 1;  // split partials: multi-row decode only
+    if (splits < 1 || (splits > 1 && a.cu_q_lens != nullptr)) return cudaErrorInvalidValue;
+    dim3 grid((a.max_q_len + R - 1) / R * splits, a.num_kv_heads, a.num_seqs);
     return dispatch_t<R>(a, dt, D, P, grid, st);
 }
 

@@ -134,6 +134,20 @@ def test_rejects_small_workspace(lib):
     assert call_decode(p, ws=None, nbytes=0) == 1
 
 
+def test_fp32_multi_row_workspace_holds_every_row(lib):
+    """fp32 K/V with several query rows: split partials per (row, q head), so
+    the workspace grows with the rows and a smaller one is refused."""
+    p1 = base_params(dtype="f32")
+    p3 = base_params(dtype="f32", decode_q_rows=3)
+    S, _ = ops.decode_plan(p3)
+    assert S > 1 and ops.decode_plan(p1)[0] == S
+    need = ops.decode_workspace_size(p3)
+    assert need >= 2 * 3 * 8 * S * (128 + 2) * 4
+    assert need > ops.decode_workspace_size(p1)
+    assert call_decode(p3, ws=FAKE, nbytes=need - 1) == 5
+    assert call_decode(p3, ws=None, nbytes=0) == 1
+
+
 def test_partial_rejects_wrong_split_count(lib):
     p = base_params()
     S, _ = ops.decode_plan(p)

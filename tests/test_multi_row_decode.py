@@ -4,7 +4,8 @@ the fp64 oracle, through the C ABI.
 Row t of T rows of a sequence of length L attends keys [0, L - T + t], the
 chunked-prefill rule, so the oracle is the one used for prefill on the same
 packed rows.  16-bit K/V run on the split-KV kernel with the rows as extra
-MMA columns, in blocks of 16 / (Hq/Hkv) rows; fp32 on the CUDA-core pass.
+MMA columns, in blocks of 16 / (Hq/Hkv) rows; fp32 on the CUDA-core pass
+over row tiles x key splits and the combine.
 """
 from __future__ import annotations
 
@@ -60,6 +61,8 @@ CASES = [
     (2, 40, 8, 128, 32, (5, 1000), 5, "f16"),             # G 5 x 5 rows: blocks of 3 and 2
     (2, 32, 2, 64, 16, (3, 200), 3, "bf16"),              # G 16: one row per block
     (2, 12, 3, 64, 16, (3, 100), 3, "f32"),               # fp32: the CUDA-core pass
+    (3, 12, 3, 64, 16, (5, 333, 1024), 5, "f32"),         # fp32: row tiles of 4 and 1, many key splits
+    (2, 32, 4, 128, 32, (16, 700), 16, "f32"),            # fp32: 16 rows, G 8
 ]
 
 
@@ -93,6 +96,27 @@ def test_multi_row_decode_short_sequence_is_flagged():
     assert status & 2  # PA_DEV_BAD_LEN
     assert np.all(got[:3] == 0)
     assert_within(got[3:], ref[3:], TOL["bf16"], "valid sequence beside an invalid one")
+
+
+def test_multi_row_decode_fp32_run_to_run_bitwise():
+    inp, meta = problem(B=2, Hq=12, Hkv=3, D=64, P=16, lens=(7, 1000), qlens=(4, 4), dt="f32",
+                        num_pages=80, seed=36)
+    a, _ = run_rows(inp, meta, 4)
+    b, _ = run_rows(inp, meta, 4)
+    assert bitwise_equal(a, b)
+
+
+@pytest.mark.parametrize("T", [2, 4])
+def test_multi_row_decode_full_size_fp32(T):
+    """Crucible's decode shape (12 q / 3 kv heads, D64, context 1024, P16,
+    fp32) with T query rows: key splits x row tiles, then the combine."""
+    wl = workloads.BY_NAME["decode_12x3_d64_L1024"]
+    inp = wl.make_inputs(q_lens=(T,) * wl.num_seqs)
+    meta = dict(num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
+                page_size=wl.page_size, scale=wl.scale, q_dtype=wl.q_dtype, kv_dtype=wl.kv_dtype)
+    got, status = run_rows(inp, meta, T)
+    assert status == 0
+    assert_within(got, oracle.attention(inp, threads=THREADS, **meta), TOL["f32"], f"fp32 T={T}")
 
 
 def test_multi_row_decode_full_size_ragged_batch():

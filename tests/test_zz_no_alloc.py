@@ -73,7 +73,7 @@ def test_noalloc_rejects_partials_beyond_the_scratch():
 
 def test_noalloc_single_split_plan():
     """Short contexts plan a single split; the scratch still holds it."""
-    inp, meta = problem(B=4, Hq=16, Hkv=4, D=128, P=32, lens=(1, 17, 40, 64), dt="f16",
+    inp, meta = problem(B=4, Hq=16, Hkv=4, D=128, P=32, lens=(1, 17, 30, 32), dt="f16",
                         num_pages=12, seed=17)
     p = _params(inp, meta)
     assert ops.decode_plan(p)[0] == 1
