@@ -826,11 +826,18 @@ __global__ void __maxnreg__(224)
 // order, so the result does not depend on timing.  At most 64 registers a
 // thread (1024/D CTAs an SM), so the CTAs that start while the partial kernel
 // runs fit beside its 256 x 224-register CTA.
-template <int D>
-__global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int P) {
-    constexpr int kBatch = 28;  // pieces loaded together
-    pdl_launch_dependents();    // the next kernel may start its own set-up
-    const int lane = threadIdx.x & 31, d = threadIdx.x;
+//
+// Head_dim 256 (warps leave ~150 pieces per q head): DS CTAs (grid y) share
+// an item's dims, and in each, NG groups of D / DS threads merge contiguous
+// runs of the pieces with their loads in flight together; group 0 merges
+// the groups' results in group order through shared memory.
+template <int D, int NG, int DS>
+__global__ void __launch_bounds__(D / DS * NG, 1024 / (D / DS * NG)) combine_v1(const V1Params a, int P) {
+    constexpr int kBatch = 28;   // pieces loaded together
+    constexpr int kDc = D / DS;  // dims of this CTA
+    pdl_launch_dependents();     // the next kernel may start its own set-up
+    const int lane = threadIdx.x & 31, dl = threadIdx.x % kDc, grp = threadIdx.x / kDc;
+    const int d = int(blockIdx.y) * kDc + dl;
     const int Tb = a.G / a.Gq;     // rows of this launch
     const int item = blockIdx.x;  // (b * Tb + t) * Hq + q head
     const int b = item / (Tb * a.Hq), rt = item % (Tb * a.Hq), t = rt / a.Hq, hq = rt % a.Hq;
@@ -861,20 +868,22 @@ __global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int 
     pdl_wait_primary();  // the partial kernel's pieces are complete from here on
     float* o = a.out + (((long long)b * a.T + a.t0 + t) * a.Hq + hq) * D + d;
     if (pb == 0) {
-        *o = 0.f;
+        if (grp == 0) *o = 0.f;
         if (h == 0 && d == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
         return;
     }
     if (np == 0) return;
     // Parts between c0 and c1 whose share is empty (possible when T < n) wrote
     // nothing: their weight is 0 and their rows are never used.
+    const int per = (np + NG - 1) / NG;  // this group's pieces: [lo, hi)
+    const int lo = min(np, grp * per), hi = min(np, lo + per);
     float M = -INFINITY, den = 0.f, num = 0.f;
-    for (int x0 = 0; x0 < np; x0 += kBatch) {
-        const int cnt = min(kBatch, np - x0);
+    for (int x0 = lo; x0 < hi; x0 += kBatch) {
+        const int cnt = min(kBatch, hi - x0);
         float mj = -INFINITY, lj = 0.f;
         if (lane < cnt) {
             const long long cc = c0 + x0 + lane;
-            if (cc * T / n != (cc + 1) * T / n) {
+            if (T >= n || cc * T / n != (cc + 1) * T / n) {  // T >= n: no share is empty
                 const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((cc + unit) * a.G + r) * 2);
                 mj = ml.x;
                 lj = ml.y;
@@ -897,7 +906,30 @@ __global__ void __launch_bounds__(D, 1024 / D) combine_v1(const V1Params a, int 
         }
         M = Mn;
     }
-    *o = den > 0.f ? num / den : 0.f;
+    if constexpr (NG == 1) {
+        *o = den > 0.f ? num / den : 0.f;
+    } else {
+        __shared__ float s_num[NG][kDc], s_m[NG], s_den[NG];
+        s_num[grp][dl] = num;
+        if (dl == 0) {
+            s_m[grp] = M;
+            s_den[grp] = den;
+        }
+        __syncthreads();
+        if (grp != 0) return;
+        float Mt = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) Mt = fmaxf(Mt, s_m[k]);
+        float nn = 0.f, dd = 0.f;
+        if (Mt != -INFINITY)
+#pragma unroll
+            for (int k = 0; k < NG; ++k) {
+                const float w = s_m[k] == -INFINITY ? 0.f : ex2(s_m[k] - Mt);
+                dd = fmaf(w, s_den[k], dd);
+                nn = fmaf(w, s_num[k][dl], nn);
+            }
+        *o = dd > 0.f ? nn / dd : 0.f;
+    }
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -972,15 +1004,17 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
     }
     if (!(phases & 2)) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(a.B) * unsigned(a.G / a.Gq) * unsigned(a.Hq));
-    cfg.blockDim = dim3(D);
+    constexpr int kGroups = D == 256 ? 4 : 1;  // piece groups of a combine CTA
+    constexpr int kSplit = D == 256 ? 4 : 1;   // CTAs per item, each with D / kSplit dims
+    cfg.gridDim = dim3(unsigned(a.B) * unsigned(a.G / a.Gq) * unsigned(a.Hq), kSplit);
+    cfg.blockDim = dim3(D / kSplit * kGroups);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_v1<D>, a, P);
+    return cudaLaunchKernelEx(&cfg, combine_v1<D, kGroups, kSplit>, a, P);
 }
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
