@@ -261,6 +261,15 @@ __device__ inline long long ctas_in_use(long long T, long long grid) {
     return want < 1 ? 1 : (want < grid ? want : grid);
 }
 
+// Warps of each CTA that take a part when warps leave their own pieces: all
+// eight unless the cost space is shorter than that, then one per cost
+// position, so that no part is empty and the combine reads no empty piece.
+// A function of the inputs and the grid alone.
+__device__ inline int warps_in_use(long long T, long long n_cta) {
+    const long long w = (T + n_cta - 1) / n_cta;
+    return int(w < 1 ? 1 : (w > kCW ? kCW : w));
+}
+
 // The load side of a warp: lane l holds page base + l of the warp's share
 // (its kv head, page id and whether it exists).
 struct LoadWindow {
@@ -305,18 +314,19 @@ __global__ void __maxnreg__(224)
 
     // ---- set-up that touches no global memory: it may overlap the kernel
     // before this one (programmatic dependent launch) ----------------------------
-    const int NH = min(a.ntiles / kCW, kMaxRing);
-    uint8_t* my_tiles = base + size_t(warp) * NH * kTile;  // [NH][kTile]
-    int* my_page = reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile) + warp * NH;
-    uint64_t* my_full =
-        reinterpret_cast<uint64_t*>(reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile) + kMaxTiles) +
-        warp * NH;
+    int* tile_page = reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile);  // [kMaxTiles]
+    uint64_t* tile_full = reinterpret_cast<uint64_t*>(tile_page + kMaxTiles);  // [kMaxTiles]
     __shared__ int s_unit[kCW][2];  // CTA merge: unit of each warp's pieces (-1: none)
     __shared__ int s_inside[kCW][2];
     __shared__ float s_w[kCtaMerge ? 8 : 1][2 * kCW];  // CTA merge: weight of each entry, per head
     __shared__ float s_md[kCtaMerge ? 8 : 1][2];       // CTA merge: max and denominator, per head
     if (lane == 0) {
-        for (int s = 0; s < NH; ++s) mbar_init(&my_full[s], 1);
+        if constexpr (kCtaMerge) {  // eight rings, each warp initialises its own
+            const int nh = min(a.ntiles / kCW, kMaxRing);
+            for (int s = 0; s < nh; ++s) mbar_init(&tile_full[warp * nh + s], 1);
+        } else {  // rings are cut once the call's size is known: every tile's barrier
+            for (int s = warp; s < a.ntiles; s += kCW) mbar_init(&tile_full[s], 1);
+        }
         mbar_fence_init();
         if (warp == 0) {
             tma_prefetch_desc(&tmK);
@@ -331,14 +341,24 @@ __global__ void __maxnreg__(224)
     const long long cost = total_cost(a, P);
     const long long n_cta = ctas_in_use(cost, gridDim.x);
     if (blockIdx.x >= n_cta) return;  // the whole CTA, before any CTA barrier
-    const long long n = n_cta * kCW;
-    const long long part = (long long)blockIdx.x * kCW + warp;
     const long long cta_s = (long long)blockIdx.x * cost / n_cta, cta_e = (blockIdx.x + 1) * cost / n_cta;
     // Small calls (short shares, few pages a warp) merge the warps' pieces in
     // the CTA, so the combine sees one piece per CTA; larger ones leave each
     // warp's pieces to the combine.  Uniform over the grid.
     const bool cta_merge = kCtaMerge && cost <= (long long)kCtaMergeMaxShare * n_cta;
-    Walk wk = walk_start(a, P, part * cost / n, (part + 1) * cost / n);
+    // Warps that take a part: with the CTA merge compiled in, a call past it
+    // has shares above 16 and all eight do.
+    const int wpc = kCtaMerge ? kCW : warps_in_use(cost, n_cta);
+    const long long n = n_cta * wpc;
+    const long long part = (long long)blockIdx.x * wpc + warp;
+    const int NH = min(a.ntiles / wpc, kMaxRing);  // ring depth of a working warp
+    const int ring = warp < wpc ? warp : 0;        // idle warps touch no ring
+    uint8_t* my_tiles = base + size_t(ring) * NH * kTile;  // [NH][kTile]
+    int* my_page = tile_page + ring * NH;
+    uint64_t* my_full = tile_full + ring * NH;
+    if constexpr (!kCtaMerge) __syncthreads();  // every tile barrier is initialised
+    Walk wk = warp < wpc ? walk_start(a, P, part * cost / n, (part + 1) * cost / n)
+                         : Walk{0, 0, 0, 0, 0, 0, 0, 0, 1};
 
     // ---- load side: issue half-stage x (page x/2 of the share; K, then V)
     // K/V are read once per call: evict-first keeps the kernel's code, the
@@ -856,7 +876,7 @@ __global__ void __launch_bounds__(D / DS * NG, 1024 / (D / DS * NG)) combine_v1(
     const int pb = seq_pages(a, b, P);
     const long long nc = ctas_in_use(T > 0 ? T : 1, a.n_ctas);
     const bool cta = a.cta_pieces && T <= (long long)kCtaMergeMaxShare * nc;  // as the partial kernel
-    const long long n = cta ? nc : nc * kCW;  // parts of the piece partition
+    const long long n = cta ? nc : nc * warps_in_use(T, nc);  // parts of the piece partition
     long long c0 = 0;
     int np = 0;
     if (pb > 0) {  // the unit's pages sit at cost positions [p0, p0 + pb)
