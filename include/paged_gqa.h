@@ -111,9 +111,9 @@ typedef struct {
                                    scheduling").  L < rows is an invalid length.
                                    16-bit K/V with automatic splits run on the
                                    split-KV kernel with the rows as extra MMA
-                                   columns, in blocks of 16 / (Hq/Hkv) rows (one
-                                   K/V pass per block; decode_phases must then
-                                   be 0 when there are several blocks); fp32 K/V
+                                   columns, in blocks of 16 / (Hq/Hkv) rows (8 /
+                                   (Hq/Hkv) at head_dim 256), each block its own
+                                   work unit of one launch; fp32 K/V
                                    take the CUDA-core pass over tiles of 4 rows
                                    x the automatic key splits, then the combine
                                    per (row, q head); num_splits must be 0.

@@ -123,8 +123,9 @@ bool use_v1(const pa_params* p) {
 // splits, at most 8 MMA columns: rows x q heads of a kv head).
 bool d256_unsupported(const pa_params* p) { return p->head_dim == 256 && !use_v1(p); }
 
-// Rows per launch of the split-KV kernel: rows x q heads of a kv head are its
-// MMA columns, at most 16; more rows take several launches, one per block.
+// Rows of a split-KV unit: rows x q heads of a kv head are its MMA columns,
+// at most 16 (8 at head_dim 256); more rows come in blocks of this many, each
+// block its own unit of the same launch.
 int row_block(const pa_params* p) {
     const int g = p->num_q_heads / p->num_kv_heads;
     const int rb = (p->head_dim == 256 ? 8 : 16) / g;
@@ -133,6 +134,9 @@ int row_block(const pa_params* p) {
 
 // The combine's grid holds one row of CTAs per (sequence, query row).
 bool rows_split_ok(const pa_params* p) { return int64_t(p->num_seqs) * decode_rows(p) <= 65535; }
+
+// Row blocks of a split-KV launch: each block of row_block rows is a unit.
+int row_blocks(const pa_params* p) { return (decode_rows(p) + row_block(p) - 1) / row_block(p); }
 
 int v1_ctas(const pa_params* p) { return p->deterministic ? kRefSms : device_sms(); }
 
@@ -211,8 +215,9 @@ PA_EXPORT size_t pa_decode_workspace_size(const pa_params* p) {
     if (check_params(p, &r) != PA_OK) return 0;
     if (d256_unsupported(p)) return 0;
     if (use_v1(p))
-        return pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads * row_block(p),
-                                             p->num_kv_heads, p->head_dim, v1_ctas(p));
+        return pa::decode_v1_workspace_bytes(p->num_seqs, p->num_kv_heads,
+                                             row_block(p) * (p->num_q_heads / p->num_kv_heads),
+                                             row_blocks(p), p->head_dim, v1_ctas(p));
     int S, tok;
     plan(p, &S, &tok);
     if (S == 1 || !rows_split_ok(p)) return 0;
@@ -272,9 +277,9 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
     if (use_v1(p)) {
         const int n = v1_ctas(p);
         const int rb = row_block(p);
-        if (rows > rb && p->decode_phases != 0) return PA_ERR_UNSUPPORTED;  // one workspace per block
-        const size_t need = pa::decode_v1_workspace_bytes(p->num_seqs, p->num_q_heads * rb,
-                                                          p->num_kv_heads, p->head_dim, n);
+        const size_t need = pa::decode_v1_workspace_bytes(p->num_seqs, p->num_kv_heads,
+                                                          rb * (p->num_q_heads / p->num_kv_heads),
+                                                          row_blocks(p), p->head_dim, n);
         if (!workspace) return PA_ERR_NULL;
         if (workspace_bytes < need) return PA_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_ALIGN;
@@ -305,13 +310,10 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         c.window = p->sliding_window;
         c.k_new = k_new;  // fused: the partial kernel writes and attends the new rows
         c.v_new = v_new;
-        for (int t0 = 0; t0 < rows; t0 += rb) {  // blocks of rows share the workspace in turn
-            c.row0 = t0;
-            c.row_count = rows - t0 < rb ? rows - t0 : rb;
-            const pa_status s = cuda_status(pa::launch_decode_v1(c, stream));
-            if (s != PA_OK) return s;
-        }
-        return PA_OK;
+        c.row0 = 0;
+        c.row_count = rows;
+        c.row_block = rb;  // blocks of rows are units of one launch
+        return cuda_status(pa::launch_decode_v1(c, stream));
     }
     if (p->sliding_window > 0) return PA_ERR_UNSUPPORTED;  // windows: split-KV kernel only
     const int phases = p->decode_phases ? p->decode_phases : 3;

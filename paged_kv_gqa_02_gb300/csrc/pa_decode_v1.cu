@@ -62,9 +62,13 @@ struct V1Params {
     uint32_t* dev_status;
     int32_t B, Hq, Hkv, G, num_pages, max_blocks, max_len;
     int32_t window;     // > 0: a row sees only its last `window` keys
-    int32_t T, t0, Gq;  // query rows per sequence, first row of this launch, q heads per kv
-                        // head.  G = rows * Gq columns per unit: column c is row
-                        // t0 + c / Gq, q head g * Gq + c % Gq
+    int32_t T, t0, Gq;  // query rows per sequence, first row of this launch, q heads per kv head
+    // Row blocks: the launch's Tl rows come in NB blocks of rb rows (the last
+    // may be shorter), each block its own unit.  Unit (b, u), u < Hv = Hkv * NB,
+    // reads kv head u / NB for rows t0 + (u % NB) * rb ...; its column c
+    // (c < G = rb * Gq) is row t0 + (u % NB) * rb + c / Gq, q head
+    // (u / NB) * Gq + c % Gq.
+    int32_t Tl, rb, NB, Hv;
     float scale_log2;
     int32_t n_ctas, ntiles, head_first, unit_cost;
     int32_t cta_pieces;  // 1: the group fits one MMA column tile, so small calls merge per CTA
@@ -111,6 +115,13 @@ __device__ inline int first_page(const V1Params& a, int L, int P) {
     return lo > 0 ? lo / P : 0;
 }
 
+// Kv head, first row and columns of unit u (a row block of a kv head).
+__device__ inline int unit_head(const V1Params& a, int u) { return a.NB == 1 ? u : u / a.NB; }
+__device__ inline int unit_row0(const V1Params& a, int u) { return a.NB == 1 ? a.t0 : a.t0 + (u % a.NB) * a.rb; }
+__device__ inline int unit_cols(const V1Params& a, int u) {
+    return a.NB == 1 ? a.G : min(a.rb, a.Tl - (u % a.NB) * a.rb) * a.Gq;
+}
+
 // Pages of sequence b that the unit reads (0: invalid length, fewer keys
 // than query rows): from first_page to the page of key L - 1.
 __device__ inline int seq_pages(const V1Params& a, int b, int P) {
@@ -119,11 +130,12 @@ __device__ inline int seq_pages(const V1Params& a, int b, int P) {
     return n > 0 ? n - first_page(a, L, P) : 0;
 }
 
-// Offset (elements) of column c of unit (b, g) in q and out: [B][T][Hq][D].
+// Offset (elements) of column c of unit (b, u) in q and out: [B][T][Hq][D].
 template <int D>
-__device__ inline long long row_off(const V1Params& a, int b, int g, int c) {
+__device__ inline long long row_off(const V1Params& a, int b, int u, int c) {
     const int tl = c / a.Gq;
-    return (((long long)b * a.T + a.t0 + tl) * a.Hq + (long long)g * a.Gq + (c - tl * a.Gq)) * D;
+    return (((long long)b * a.T + unit_row0(a, u) + tl) * a.Hq + (long long)unit_head(a, u) * a.Gq +
+            (c - tl * a.Gq)) * D;
 }
 
 // A warp's position in its share of the cost space.
@@ -159,7 +171,7 @@ __device__ inline long long total_cost(const V1Params& a, int P) {
     long long tot = 0;
     for (int b = threadIdx.x & 31; b < a.B; b += 32) {
         const int pb = seq_pages(a, b, P);
-        if (pb > 0) tot += (long long)a.Hkv * (pb + a.unit_cost);
+        if (pb > 0) tot += (long long)a.Hv * (pb + a.unit_cost);
     }
     return warp_sum_ll(tot);
 }
@@ -173,7 +185,7 @@ __device__ inline Walk walk_start(const V1Params& a, int P, long long s, long lo
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int b = b0 + lane;
         const int pb = b < a.B ? seq_pages(a, b, P) : 0;
-        const long long c = pb > 0 ? (long long)a.Hkv * (pb + W) : 0;
+        const long long c = pb > 0 ? (long long)a.Hv * (pb + W) : 0;
         const long long incl = warp_incl_scan_ll(c, lane);
         const long long total = __shfl_sync(0xffffffffu, incl, 31);
         if (s < basep + total) {
@@ -200,7 +212,7 @@ __device__ inline Walk walk_start(const V1Params& a, int P, long long s, long lo
 // Moves to the next unit with pages; done once its pages start at or after e.
 __device__ inline void walk_next_unit(Walk& w, const V1Params& a, int P) {
     w.start += w.pb + a.unit_cost;
-    if (++w.g == a.Hkv) {
+    if (++w.g == a.Hv) {
         w.g = 0;
         int pb = 0;
         do {
@@ -387,7 +399,8 @@ __global__ void __maxnreg__(224)
             mbar_arrive_expect_tx(&my_full[slot], ok ? kTile : 0);
             if (ok) {
                 uint8_t* dst = my_tiles + size_t(slot) * kTile;
-                const int xc = a.head_first ? g : 0, yc = a.head_first ? 0 : g;
+                const int gh = unit_head(a, g);
+                const int xc = a.head_first ? gh : 0, yc = a.head_first ? 0 : gh;
 #pragma unroll
                 for (int hh = 0; hh < kHalves; ++hh)
                     tma_load_4d_hint(dst + hh * P * 128, (hx & 1) ? &tmV : &tmK, &my_full[slot], 64 * hh, xc,
@@ -422,29 +435,24 @@ __global__ void __maxnreg__(224)
     float sc[kMt][NT][4];
     // B fragments of Q^T for unit (b, g): column n = nt*8 + g4 (0 past G)
     auto load_q = [&](uint32_t (&dst)[NT][kKs][2], int b, int g) {
+        const int Gu = unit_cols(a, g);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int h = nt * 8 + g4;
             const uint32_t* row =
-                reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.q) + row_off<D>(a, b, g, h < G ? h : 0));
+                reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.q) + row_off<D>(a, b, g, h < Gu ? h : 0));
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
-                dst[nt][ks][0] = h < G ? __ldg(row + 8 * ks + t4) : 0u;
-                dst[nt][ks][1] = h < G ? __ldg(row + 8 * ks + 4 + t4) : 0u;
+                dst[nt][ks][0] = h < Gu ? __ldg(row + 8 * ks + t4) : 0u;
+                dst[nt][ks][1] = h < Gu ? __ldg(row + 8 * ks + 4 + t4) : 0u;
             }
         }
     };
     if (!wk.done) load_q(qn, wk.b, wk.g);
     // Causal lag of the columns this lane holds (heads nt*8 + 2*t4 + j): row t
-    // of T sees keys [0, L - (T - 1 - t)).  Padding columns take no lag.
+    // of T sees keys [0, L - (T - 1 - t)).  Padding columns take no lag.  Set
+    // per unit (its row block).
     int lag[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int c = nt * 8 + 2 * t4 + j;
-            lag[nt][j] = c < G ? a.T - 1 - (a.t0 + c / a.Gq) : 0;
-        }
     int x = 0;  // half-stage number
     // CTA merge (one q-head column tile): the share's first piece, when it is
     // not whole and other units follow, waits here; its last non-whole piece
@@ -455,6 +463,17 @@ __global__ void __maxnreg__(224)
 
     while (!wk.done) {
         const int L = __ldg(a.context_lens + wk.b);
+        const int Gu = unit_cols(a, wk.g);  // this unit's columns
+        {
+            const int r0u = unit_row0(a, wk.g);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int c = nt * 8 + 2 * t4 + j;
+                    lag[nt][j] = c < Gu ? a.T - 1 - (r0u + c / a.Gq) : 0;
+                }
+        }
         const int fp = first_page(a, L, P);  // page i of the unit is page fp + i of the sequence
         const bool whole = (wk.pf == 0) && (wk.pe == wk.pb);
 #pragma unroll
@@ -492,7 +511,7 @@ __global__ void __maxnreg__(224)
             const bool valid = ok && my_page[x % NH] >= 0;
             const bool app = a.k_new != nullptr && i == wk.pb - 1;  // the unit's last page holds row L - 1
             if (valid && app)
-                append_row<D, P>(my_tiles + size_t(x % NH) * kTile, a.k_new, a.k_cache, a, wk.b, wk.g,
+                append_row<D, P>(my_tiles + size_t(x % NH) * kTile, a.k_new, a.k_cache, a, wk.b, unit_head(a, wk.g),
                                  my_page[x % NH], ntok - 1);
             if (valid) {
                 const uint32_t kb = smem_u32(my_tiles + size_t(x % NH) * kTile);
@@ -600,7 +619,8 @@ __global__ void __maxnreg__(224)
             }
             if (valid && ok) {
                 uint8_t* vt = my_tiles + size_t(x % NH) * kTile;
-                if (app) append_row<D, P>(vt, a.v_new, a.v_cache, a, wk.b, wk.g, my_page[x % NH], ntok - 1);
+                if (app)
+                    append_row<D, P>(vt, a.v_new, a.v_cache, a, wk.b, unit_head(a, wk.g), my_page[x % NH], ntok - 1);
                 // keys before every row's window in the first window page are
                 // never read: zero their V rows (0 * NaN would poison P V)
                 const int vlo = a.window > 0 && i == 0 ? L - a.T + a.t0 - a.window + 1 - fp * P : 0;
@@ -654,14 +674,14 @@ __global__ void __maxnreg__(224)
                 v += __shfl_xor_sync(0xffffffffu, v, 16);
                 lrun[nt][j] = v;
             }
-        const int unit = wk.b * a.Hkv + wk.g;
+        const int unit = wk.b * a.Hv + wk.g;
         if (whole) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int h = nt * 8 + 2 * t4 + j;
-                    if (h < G) {
+                    if (h < Gu) {
                         float* ob = a.out + row_off<D>(a, wk.b, wk.g, h);
                         const float inv = lrun[nt][j] > 0.f ? 1.f / lrun[nt][j] : 0.f;
 #pragma unroll
@@ -778,7 +798,7 @@ __global__ void __maxnreg__(224)
             const int u = __shfl_sync(0xffffffffu, su, e);
             const uint32_t emask = __ballot_sync(0xffffffffu, su == u) & 0xffffu;
             const bool inside = s_inside[e >> 1][e & 1] != 0;
-            const int ub = u / a.Hkv, ug = u % a.Hkv;
+            const int ub = u / a.Hv, ug = u % a.Hv;
             // Weights: warp w takes heads 2w and 2w + 1, one lane per entry;
             // maxima and denominators by fixed 16-lane shuffle trees.
             if (2 * warp < G) {
@@ -822,8 +842,9 @@ __global__ void __maxnreg__(224)
                 const float M = s_md[h][0], den = s_md[h][1];
                 if (inside) {
                     const float inv = den > 0.f ? 1.f / den : 0.f;
-                    *reinterpret_cast<float4*>(a.out + row_off<D>(a, ub, ug, h) + d4) =
-                        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+                    if (h < unit_cols(a, ug))
+                        *reinterpret_cast<float4*>(a.out + row_off<D>(a, ub, ug, h) + d4) =
+                            make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
                 } else {
                     const long long slot = (long long)blockIdx.x + u;
                     *reinterpret_cast<float4*>(a.ws_acc + (slot * G + h) * D + d4) = num;
@@ -858,16 +879,18 @@ __global__ void __launch_bounds__(D / DS * NG, 1024 / (D / DS * NG)) combine_v1(
     pdl_launch_dependents();     // the next kernel may start its own set-up
     const int lane = threadIdx.x & 31, dl = threadIdx.x % kDc, grp = threadIdx.x / kDc;
     const int d = int(blockIdx.y) * kDc + dl;
-    const int Tb = a.G / a.Gq;     // rows of this launch
+    const int Tb = a.Tl;           // rows of this launch
     const int item = blockIdx.x;  // (b * Tb + t) * Hq + q head
     const int b = item / (Tb * a.Hq), rt = item % (Tb * a.Hq), t = rt / a.Hq, hq = rt % a.Hq;
-    const int g = hq / a.Gq, r = t * a.Gq + hq % a.Gq, h = hq;  // r: the unit's column
-    const int unit = b * a.Hkv + g;
+    const int k = t / a.rb;                             // row block
+    const int g = (hq / a.Gq) * a.NB + k;               // unit within the sequence
+    const int r = (t - k * a.rb) * a.Gq + hq % a.Gq, h = hq;  // r: the unit's column
+    const int unit = b * a.Hv + g;
     const int W = a.unit_cost;
     long long T = 0, pre = 0;
     for (int x = lane; x < a.B; x += 32) {
         const int pg = seq_pages(a, x, P);
-        const long long c = pg > 0 ? (long long)a.Hkv * (pg + W) : 0;
+        const long long c = pg > 0 ? (long long)a.Hv * (pg + W) : 0;
         T += c;
         if (x < b) pre += c;
     }
@@ -1026,7 +1049,7 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
     cudaLaunchConfig_t cfg = {};
     constexpr int kGroups = D == 256 ? 4 : 1;  // piece groups of a combine CTA
     constexpr int kSplit = D == 256 ? 4 : 1;   // CTAs per item, each with D / kSplit dims
-    cfg.gridDim = dim3(unsigned(a.B) * unsigned(a.G / a.Gq) * unsigned(a.Hq), kSplit);
+    cfg.gridDim = dim3(unsigned(a.B) * unsigned(a.Tl) * unsigned(a.Hq), kSplit);
     cfg.blockDim = dim3(D / kSplit * kGroups);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1039,13 +1062,13 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: (m, l) pairs, then accumulators, one slot per (part, unit) piece.
+// Workspace: (m, l) pairs, then accumulators, one slot per (part, unit) piece
+// of G columns; Hv units per sequence.
 struct WsLayout {
     size_t ml, acc, total;
 };
-WsLayout ws_layout(int B, int Hq, int Hkv, int D, int n_ctas) {
-    const size_t slots = size_t(n_ctas) * kCW + size_t(B) * Hkv;
-    const size_t G = size_t(Hq / Hkv);
+WsLayout ws_layout(int B, int Hv, int G, int D, int n_ctas) {
+    const size_t slots = size_t(n_ctas) * kCW + size_t(B) * Hv;
     WsLayout w;
     w.ml = 0;
     w.acc = w.ml + round256(slots * G * 2 * sizeof(float));
@@ -1055,8 +1078,8 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int D, int n_ctas) {
 
 }  // namespace
 
-size_t decode_v1_workspace_bytes(int B, int Hq, int Hkv, int D, int n_ctas) {
-    return ws_layout(B, Hq, Hkv, D, n_ctas).total;
+size_t decode_v1_workspace_bytes(int B, int Hkv, int G, int NB, int D, int n_ctas) {
+    return ws_layout(B, Hkv * NB, G, D, n_ctas).total;
 }
 
 cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
@@ -1104,9 +1127,11 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.out = call.out;
     const int T = call.rows > 0 ? call.rows : 1;
     const int nr = call.row_count > 0 ? call.row_count : T;  // rows of this launch
-    const int G = nr * (call.Hq / call.Hkv);  // columns per unit: rows x q heads of a kv head
+    const int rb = call.row_block > 0 && call.row_block < nr ? call.row_block : nr;  // rows of a unit
+    const int NB = (nr + rb - 1) / rb;
+    const int G = rb * (call.Hq / call.Hkv);  // columns per unit: rows x q heads of a kv head
     if (G > 16 || call.row0 < 0 || call.row0 + nr > T) return cudaErrorInvalidValue;
-    const WsLayout wl = ws_layout(call.B, nr * call.Hq, call.Hkv, D, call.n_ctas);
+    const WsLayout wl = ws_layout(call.B, call.Hkv * NB, G, D, call.n_ctas);
     char* ws = static_cast<char*>(call.workspace);
     a.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
     a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
@@ -1117,6 +1142,10 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.G = G;
     a.T = T;
     a.t0 = call.row0;
+    a.Tl = nr;
+    a.rb = rb;
+    a.NB = NB;
+    a.Hv = call.Hkv * NB;
     a.Gq = call.Hq / call.Hkv;
     a.num_pages = call.num_pages;
     a.max_blocks = call.max_blocks;

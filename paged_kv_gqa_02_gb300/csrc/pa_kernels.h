@@ -32,7 +32,9 @@ struct DecodeV1Call {
     int phases;  // bit 0: partial kernel, bit 1: combine kernel
     int rows = 1;       // query rows per sequence (causal among them)
     int row0 = 0;       // first row this launch handles
-    int row_count = 0;  // rows this launch handles (0: all); row_count x Hq/Hkv <= 16
+    int row_count = 0;  // rows this launch handles (0: all)
+    int row_block = 0;  // rows of a unit (0: row_count); row_block x Hq/Hkv <= 16.  The
+                        // launch's rows come in blocks of row_block, each block a unit
     int window = 0;     // > 0: each row sees only its last `window` keys
     // KV append (both nullptr: none): [B][Hkv][D] rows written to row L_b - 1
     // of the cache and attended in place of what it held
@@ -52,7 +54,8 @@ cudaError_t launch_append_kv(const void* k_new, const void* v_new, void* k_cache
                              int64_t token_stride, int64_t head_stride, cudaStream_t st);
 
 // Hq counts q heads times query rows per sequence.
-size_t decode_v1_workspace_bytes(int B, int Hq, int Hkv, int D, int n_ctas);
+// Workspace of a launch whose units have G columns, NB row blocks per kv head.
+size_t decode_v1_workspace_bytes(int B, int Hkv, int G, int NB, int D, int n_ctas);
 cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st);
 
 }  // namespace pa

@@ -258,10 +258,10 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
 // Combine: one CTA per (q head, sequence), one thread per output dim.
 __global__ void combine_v0(const float* __restrict__ ml, const float* __restrict__ acc,
                            float* __restrict__ out, int Hq, int S, int D) {
-    // Batches of 16 splits: lane j holds split x0 + j's (m, l), every thread
-    // loads its dim of all 16 accumulators at once; batches are merged by
+    // Batches of 32 splits: lane j holds split x0 + j's (m, l), every thread
+    // loads its dim of all 32 accumulators at once; batches are merged by
     // rescaling in ascending split order (fixed shuffle trees, no atomics).
-    constexpr int kB = 16;
+    constexpr int kB = 32;
     pdl_launch_dependents();
     pdl_wait_primary();  // the partials are complete from here on
     const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31;

@@ -98,6 +98,28 @@ def test_multi_row_decode_short_sequence_is_flagged():
     assert_within(got[3:], ref[3:], TOL["bf16"], "valid sequence beside an invalid one")
 
 
+def test_multi_row_decode_phases_split_the_call():
+    """decode_phases 1 then 2 on one workspace gives the single call's result
+    bit for bit, with the rows in two blocks (G 8 x 4 rows) of one launch."""
+    inp, meta = problem(B=2, Hq=32, Hkv=4, D=128, P=32, lens=(9, 900), qlens=(4, 4), dt="bf16",
+                        num_pages=40, seed=37)
+    whole, _ = run_rows(inp, meta, 4)
+    bt = inp["block_tables"]
+    p = ops.make_params(num_seqs=2, num_q_heads=32, num_kv_heads=4, head_dim=128, page_size=32,
+                        num_pages=int(inp["num_pages"]), max_blocks_per_seq=bt.shape[1],
+                        max_context_len=bt.shape[1] * 32, scale=meta["scale"], dtype="bf16",
+                        kv_dtype="bf16", decode_q_rows=4)
+    d = ops.device_inputs(inp, "bf16")
+    ws = torch.empty(ops.decode_workspace_size(p), dtype=torch.uint8, device="cuda")
+    out = torch.full((8, 32, 128), float("nan"), dtype=torch.float32, device="cuda")
+    for ph in (1, 2):
+        p.decode_phases = ph
+        ops.decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], out=out,
+                   workspace=ws)
+    torch.cuda.synchronize()
+    assert bitwise_equal(out.cpu().numpy(), whole)
+
+
 def test_multi_row_decode_fp32_run_to_run_bitwise():
     inp, meta = problem(B=2, Hq=12, Hkv=3, D=64, P=16, lens=(7, 1000), qlens=(4, 4), dt="f32",
                         num_pages=80, seed=36)
