@@ -871,7 +871,8 @@ __global__ void __maxnreg__(224)
 // Head_dim 256 (warps leave ~150 pieces per q head): DS CTAs (grid y) share
 // an item's dims, and in each, NG groups of D / DS threads merge contiguous
 // runs of the pieces with their loads in flight together; group 0 merges
-// the groups' results in group order through shared memory.
+// the groups' results in group order through shared memory.  A CTA keeps to
+// 128 threads of 64 registers: one then fits beside a partial-kernel CTA.
 template <int D, int NG, int DS>
 __global__ void __launch_bounds__(D / DS * NG, 1024 / (D / DS * NG)) combine_v1(const V1Params a, int P) {
     constexpr int kBatch = 28;   // pieces loaded together
@@ -1047,8 +1048,12 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
     }
     if (!(phases & 2)) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
+    // Every combine CTA has 128 threads at most (8,192 registers), so one fits
+    // beside a partial-kernel CTA and the next call's partial CTAs find room
+    // beside the combine's.  D 256: eight CTAs an item, each with 32 dims and
+    // four piece groups of one warp.
     constexpr int kGroups = D == 256 ? 4 : 1;  // piece groups of a combine CTA
-    constexpr int kSplit = D == 256 ? 4 : 1;   // CTAs per item, each with D / kSplit dims
+    constexpr int kSplit = D == 256 ? 8 : 1;   // CTAs per item, each with D / kSplit dims
     cfg.gridDim = dim3(unsigned(a.B) * unsigned(a.Tl) * unsigned(a.Hq), kSplit);
     cfg.blockDim = dim3(D / kSplit * kGroups);
     cfg.stream = st;
