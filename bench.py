@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -65,11 +66,19 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"' + r"|'(?:\\.|[^'\\])*'" + r"|//[^\n]*|/\*.*?\*/", re.S)
+
+
 def src_hash():
+    """Hash of the kernel sources without their comments and with runs of
+    white space collapsed: editing a comment leaves the compiled kernels, and
+    so the ncu counters taken on them, as they were."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "paged_kv_gqa_02_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            text = fh.read()
+        code = _TOKENS.sub(lambda m: " " if m.group(0).startswith("/") else m.group(0), text)
+        h.update(os.path.basename(f).encode() + b"\0" + " ".join(code.split()).encode() + b"\0")
     return h.hexdigest()[:12]
 
 

@@ -274,9 +274,10 @@ __device__ inline long long ctas_in_use(long long T, long long grid) {
 }
 
 // Warps of each CTA that take a part when warps leave their own pieces: all
-// eight unless the cost space is shorter than that, then one per cost
-// position, so that no part is empty and the combine reads no empty piece.
-// A function of the inputs and the grid alone.
+// eight unless the cost space is shorter than that, then about one per cost
+// position (rounded up, so at most n_cta - 1 parts are empty), which spares
+// the combine the mostly empty pieces of eight parts a CTA.  A function of
+// the inputs and the grid alone.
 __device__ inline int warps_in_use(long long T, long long n_cta) {
     const long long w = (T + n_cta - 1) / n_cta;
     return int(w < 1 ? 1 : (w > kCW ? kCW : w));
