@@ -83,3 +83,63 @@ def test_cost_partition(seed):
         assert got == want
         whole = [(pf == 0 and pe == pb) for _, pf, pe in per_unit[u]]
         assert any(whole) == (c0 == c1) == (len(got) == 1)
+
+
+# The kernels' own part count: CTAs in use = min(grid, ceil(T / 3)); eight
+# warp parts a CTA with the in-CTA merge compiled in, else
+# clamp(ceil(T / n_cta), 1, 8).  Both can exceed T (empty parts), which the
+# combine must skip.  Row blocks are extra units: (b, kv head, block).
+MIN_CTA_COST, CW = 3, 8
+
+
+def kernel_parts(T, grid, cta_merge_variant):
+    n_cta = max(1, min(grid, (T + MIN_CTA_COST - 1) // MIN_CTA_COST))
+    wpc = CW if cta_merge_variant else max(1, min(CW, (T + n_cta - 1) // n_cta))
+    return n_cta, n_cta * wpc
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_kernel_part_counts_locate_every_piece(seed):
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 20))
+    Hkv = int(rng.integers(1, 9))
+    NB = int(rng.choice([1, 1, 2, 3]))  # row blocks as units
+    grid = int(rng.choice([4, 37, 152]))
+    merge = bool(rng.integers(0, 2))
+    W = 2
+    pages = [int(x) for x in rng.integers(0, 40, size=B)]
+    pages = [p if rng.random() > 0.1 else 0 for p in pages]
+    units, start = [], 0
+    for b in range(B):
+        for g in range(Hkv * NB):
+            units.append((start, pages[b]))
+            if pages[b]:
+                start += W + pages[b]
+    T = start
+    if T == 0:
+        return
+    n_cta, n = kernel_parts(T, grid, merge)
+    assert n_cta <= grid and n <= n_cta * CW
+    shares = [(v * T // n, (v + 1) * T // n) for v in range(n)]
+    # CTA c's share is the union of its warps' shares
+    for c in range(n_cta):
+        w = n // n_cta
+        assert shares[c * w][0] == c * T // n_cta and shares[c * w + w - 1][1] == (c + 1) * T // n_cta
+    covered, per_unit = {}, {}
+    for v, sh in enumerate(shares):
+        for (u, pf, pe) in walk(sh, units, W):
+            for i in range(pf, pe):
+                assert (u, i) not in covered
+                covered[(u, i)] = v
+            per_unit.setdefault(u, []).append(v)
+            assert v + u < n_cta * CW + len(units)  # workspace slot
+    for u, (ustart, pb) in enumerate(units):
+        if pb == 0:
+            continue
+        assert all((u, i) in covered for i in range(pb))
+        p0 = ustart + W
+        c0, c1 = owner(p0, T, n), owner(p0 + pb - 1, T, n)
+        nonempty = [v for v in range(c0, c1 + 1) if (v * T // n) != ((v + 1) * T // n)]
+        assert per_unit[u] == nonempty
+        if T >= n:  # the combine's shortcut: no share is empty
+            assert nonempty == list(range(c0, c1 + 1))
