@@ -164,9 +164,11 @@ size_t pa_decode_workspace_size(const pa_params *p);
  * With num_splits = 0 and 16-bit K/V the partition is length-balanced: one
  * persistent CTA per SM (a fixed 152 when deterministic = 1, the device's
  * SM count otherwise; 8 warps each) takes equal contiguous shares of the
- * ordered (sequence, kv head, page) list, each warp one share; units that
- * fall inside one share are finished there, and a second kernel merges the
- * pieces of the others in ascending share order.  Otherwise the fixed split
+ * ordered (sequence, kv head [, row block], page) list, and its warps split
+ * the share the same way (fewer warps for small calls when the group needs
+ * two MMA column tiles or head_dim is 256); units that fall inside one
+ * share are finished there, and a second kernel merges the pieces of the
+ * others in ascending share order.  Otherwise the fixed split
  * plan of pa_decode_plan is used (the pa_decode_partial + pa_combine pair). */
 pa_status pa_decode(const pa_params *p, const void *q, const void *k_cache,
                     const void *v_cache, const int32_t *block_tables,
@@ -229,9 +231,14 @@ pa_status pa_combine(const pa_params *p, const float *partial_ml, const float *p
  * serving loop that forbids allocation after start-up, or a process whose
  * caching allocator already holds the free memory).
  *
- * It computes exactly what pa_decode computes, with the same kernels, but
- * keeps the split partials in a static device array of
- * PA_NOALLOC_SCRATCH_BYTES inside the library.  Every GPU that loads the
+ * It runs the fixed split plan of pa_decode_plan (pa_decode_partial, then
+ * pa_combine: the path pa_decode takes when num_splits is set), keeping the
+ * split partials in a static device array of PA_NOALLOC_SCRATCH_BYTES
+ * inside the library.  Its result equals pa_decode's within the decode
+ * tolerances; where pa_decode takes the same plan (fp32 K/V with several
+ * splits, or num_splits > 0) both run the same kernels.  Several query rows,
+ * sliding windows and head_dim 256 return PA_ERR_UNSUPPORTED, as for
+ * pa_decode_partial.  Every GPU that loads the
  * library holds that array until the process exits.  It allocates nothing
  * and calls no allocating routine.
  *  - Limit: when the plan's partials (B * Hq * S * (D + 2) floats, each part
