@@ -134,6 +134,41 @@ def test_rejects_small_workspace(lib):
     assert call_decode(p, ws=None, nbytes=0) == 1
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(decode_q_rows=17), 2),                                  # more rows than supported
+    (dict(decode_q_rows=-1), 2),
+    (dict(decode_q_rows=9, max_context_len=8), 2),                # rows beyond the capacity
+    (dict(sliding_window=-1), 2),
+    (dict(dtype="f32", sliding_window=8), 6),                     # windows: split-KV kernel only
+    (dict(num_splits=2, sliding_window=8), 6),
+    (dict(head_dim=256, num_q_heads=32, num_kv_heads=2), 6),      # D 256 with 16 heads a kv head
+    (dict(head_dim=256, num_splits=2), 6),                        # D 256 off the split-KV kernel
+])
+def test_rejects_unsupported_decode_options(lib, kw, code):
+    assert call_decode(base_params(**kw)) == code
+
+
+def test_partial_and_append_reject_several_rows(lib):
+    p = base_params(decode_q_rows=2)
+    S, _ = ops.decode_plan(p)
+    assert lib.pa_decode_partial(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, S,
+                                 None, None) == 6
+    assert ops.load().pa_decode_append(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                       None, 0, None, None) == 6
+
+
+def test_row_block_workspace_holds_every_block(lib):
+    """16-bit K/V, 8 q heads a kv head, 4 rows: two row blocks of 2 rows are
+    units of one launch, each with 16 columns, so the workspace holds a slot
+    per (part, unit) for 2 x num_kv_heads units a sequence."""
+    p = base_params(num_q_heads=32, num_kv_heads=4, decode_q_rows=4)
+    need = ops.decode_workspace_size(p)
+    slots = 152 * 8 + 2 * 4 * 2
+    assert need >= slots * 16 * (128 + 2) * 4
+    assert need > ops.decode_workspace_size(base_params(num_q_heads=32, num_kv_heads=4))
+    assert call_decode(p, ws=FAKE, nbytes=need - 1) == 5
+
+
 def test_fp32_multi_row_workspace_holds_every_row(lib):
     """fp32 K/V with several query rows: split partials per (row, q head), so
     the workspace grows with the rows and a smaller one is refused."""
