@@ -858,7 +858,7 @@ __global__ void __maxnreg__(224)
 }
 
 // Merges the pieces of units that span several parts: one CTA per (sequence,
-// q head), one thread per output dim.  The CTA locates its pieces from the
+// row, q head), one thread per output dim (head_dim 256: see below).  The CTA locates its pieces from the
 // lengths alone (a lane-parallel prefix over the sequences) before it waits
 // for the partial kernel through programmatic dependent launch; after the
 // wait, the (m, l) pairs of up to 28 pieces (one per lane) and their
