@@ -3,12 +3,14 @@
 // Work partition (split-KV, crucible README "Split-position attention";
 // minfer doc 71: all q heads of a kv head share each K/V tile).  The work of
 // a call is the ordered list of (sequence, kv head) units, unit (b, g) made of
-// the pages of sequence b read for kv head g.  In a cost space where each
+// the pages of sequence b read for kv head g (with several query rows, one
+// unit per row block of a kv head).  In a cost space where each
 // unit occupies unit_cost + pages positions (unit_cost stands for the fixed
 // work of a unit piece: its query row and its result), the n CTAs in use
 // (all of the persistent grid unless the call is tiny) take equal contiguous
 // shares [c*T/n, (c+1)*T/n), and the 8 warps of a CTA split its share the
-// same way.  Every warp therefore moves about the same number of bytes
+// same way (fewer warps in small calls without the in-CTA merge).  Every
+// working warp therefore moves about the same number of bytes
 // whatever the mix of context lengths, and the grid does not depend on
 // device data.  A warp finishes a unit that lies inside its part.  When the
 // group's q heads fit one 8-wide MMA column tile, the warps of a CTA then
@@ -267,7 +269,8 @@ __device__ inline void split_hi_lo(float x, float y, uint32_t& hi, uint32_t& lo)
 // CTAs that take a share: all of them unless the call is so small that a
 // share would fall below kMinCtaCost.  A function of the inputs and the grid
 // alone.  CTA c owns [c*T/n, (c+1)*T/n) of the cost space; its warp w owns
-// the matching eighth, part c*8 + w of the n*8 warp parts.
+// the matching eighth, part c*8 + w of the n*8 warp parts (or, with wpc
+// working warps a CTA, the matching wpc-th, part c*wpc + w).
 __device__ inline long long ctas_in_use(long long T, long long grid) {
     const long long want = (T + kMinCtaCost - 1) / kMinCtaCost;
     return want < 1 ? 1 : (want < grid ? want : grid);
