@@ -2,13 +2,14 @@
 // kv head, sequence), all q heads of the kv head in the CTA so each K/V page
 // row is read from HBM once per kv head (minfer doc 71: the GQA-batched
 // shape; crucible results: one CTA shares K/V across the q heads of one kv
-// head).  CUDA-core fp32 arithmetic, synchronous 16-byte page-row loads,
-// online softmax per page (crucible results, the online-softmax
-// experiment), base-2 exponentials.
+// head).  CUDA-core fp32 arithmetic, 16-byte page-row loads staged through
+// registers one page ahead, online softmax per page (crucible results, the
+// online-softmax experiment), base-2 exponentials.
 //
-// It serves three roles: the decode split partial (R = 1 row per sequence),
-// the chunked-prefill kernel (R rows per tile, causal per row), and the
-// fp32-KV decode path.  The split combine is at the end of this file.
+// It serves four roles: the decode split partial (R = 1 row per sequence),
+// the chunked-prefill kernel (R rows per tile, causal per row), the
+// multi-row decode split partial (row tiles x key splits), and the fp32-KV
+// decode path.  The split combine is at the end of this file.
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 #include "pa_ptx.cuh"
