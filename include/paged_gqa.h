@@ -22,7 +22,9 @@
  *  - Ownership: every pointer argument is device memory owned by the caller
  *    (except `const pa_params*`, which is host memory read during the call).
  *    The library allocates nothing and keeps no per-call state; the only
- *    global memory it uses besides the arguments is the caller's workspace.
+ *    global memory it uses besides the arguments is the caller's workspace
+ *    (one exception: pa_decode_noalloc keeps its split partials in a static
+ *    device array of PA_NOALLOC_SCRATCH_BYTES inside the library).
  *  - Asynchrony: calls enqueue work on `stream` and return.  PA_OK means the
  *    arguments passed host validation and the kernels were launched.
  *    Host-detectable errors return before anything is launched.

@@ -46,7 +46,7 @@ namespace {
 
 constexpr int kCW = 8;                        // warps per CTA, each a partition part
 constexpr int kThreadsV1 = kCW * 32;
-constexpr uint32_t kWaitLimit = 1u << 22;     // polls before a wait gives up
+constexpr uint64_t kWaitNs = 2000000000ull;   // a wait gives up after 2 s of the global timer
 constexpr int kMaxTiles = 64;                 // page tiles (half-stages) per CTA, at most
 constexpr int kMaxRing = 16;                  // page tiles in one warp's ring, at most
 constexpr int kSmemLimit = 232448;            // 227 KiB opt-in per CTA
@@ -382,7 +382,11 @@ __global__ void __maxnreg__(224)
     const uint64_t kv_policy = l2_policy_evict_first();
     LoadWindow lw{wk, wk.pf, 0, 0, 0, -1};
     if (!wk.done) window_fill(lw, a, P);
+    // Half-stages [0, n_issued) have been issued (the live pages of a share
+    // form a prefix); after a wait gives up at half-stage x_stop, no more are
+    // issued and [x_stop, n_issued) may still be in flight.
     bool timed_out = false;
+    int n_issued = 0, x_stop = 0;
     auto issue = [&](int hx) {
         const int j = hx >> 1;
         while (j >= lw.base + 32) {  // next 32 pages of the share
@@ -395,6 +399,7 @@ __global__ void __maxnreg__(224)
         const int g = __shfl_sync(0xffffffffu, lw.g, src);
         const int pg = __shfl_sync(0xffffffffu, lw.page, src);
         if (!live) return;
+        n_issued = hx + 1;
         if (lane == 0) {
             const int slot = hx % NH;
             const bool ok = pg >= 0 && pg < a.num_pages;
@@ -507,8 +512,10 @@ __global__ void __maxnreg__(224)
             const int ntok = min(P, rem);
             // ---- K tile: S^T = K Q^T, masked, online softmax
             bool ok = !timed_out;
-            if (ok && !mbar_wait(&my_full[x % NH], (x / NH) & 1, kWaitLimit)) {
+            // every lane waits (each needs the barrier's ordering); one verdict per warp
+            if (ok && !__all_sync(0xffffffffu, mbar_wait_ns(&my_full[x % NH], (x / NH) & 1, kWaitNs))) {
                 timed_out = true;
+                x_stop = x;
                 ok = false;
                 if (lane == 0) flag(a.dev_status, PA_DEV_TIMEOUT);
             }
@@ -616,8 +623,9 @@ __global__ void __maxnreg__(224)
             }
             // ---- V tile: O^T += V^T P^T
             ok = !timed_out;
-            if (ok && !mbar_wait(&my_full[x % NH], (x / NH) & 1, kWaitLimit)) {
+            if (ok && !__all_sync(0xffffffffu, mbar_wait_ns(&my_full[x % NH], (x / NH) & 1, kWaitNs))) {
                 timed_out = true;
+                x_stop = x;
                 ok = false;
                 if (lane == 0) flag(a.dev_status, PA_DEV_TIMEOUT);
             }
@@ -737,11 +745,19 @@ __global__ void __maxnreg__(224)
         if (nx.done) break;  // o / mrun / lrun keep the last piece
         wk = nx;
     }
-    // A wait that gave up may leave copies in flight: wait (bounded) for them.
-    if (timed_out && lane == 0)
-        for (int s = 0; s < NH; ++s) mbar_wait(&my_full[s], ((x + s) / NH) & 1, 1024);
+    // A wait that gave up leaves half-stages [x_stop, n_issued) (at most NH)
+    // possibly in flight: wait for each of them, bounded by the global timer,
+    // before the ring is reused for the merge or the CTA exits.  A copy that
+    // still has not landed keeps this warp's ring out of the merge.
+    bool ring_free = true;
+    if (timed_out) {
+        for (int y = x_stop; y < n_issued; ++y)
+            ring_free = mbar_wait_ns(&my_full[y % NH], (y / NH) & 1, kWaitNs) && ring_free;
+        ring_free = __all_sync(0xffffffffu, ring_free);
+    }
     __syncwarp();
     if (kCtaMerge && cta_merge) {
+        if (!ring_free) first_unit = last_unit = -1;  // nothing is staged in a ring still being written
         // Stage the non-whole pieces in this warp's own ring (its copies are
         // all consumed): piece k is [G][D + 4] accumulators (the pad puts the
         // 8 x 4 lanes of one store in 32 distinct banks) then [G] (m, l) pairs.

@@ -42,7 +42,8 @@ struct DecodeV1Call {
     const void* v_new = nullptr;
 };
 // Chunked prefill on the tensor cores (tcgen05): 16-bit Q/K/V, head_dim 128,
-// pages of 16 or 32 slots, G = Hq/Hkv <= 16, scale > 0.  Grid (Hkv * B, row tiles).
+// pages of 16 or 32 slots, G = Hq/Hkv <= 16, scale > 0.  One CTA per (row-tile
+// pair, kv head, sequence), the pairs of a (sequence, kv head) consecutive.
 bool prefill_tc_supported(pa_dtype dt, int D, int P, int G, float scale);
 cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st);
 

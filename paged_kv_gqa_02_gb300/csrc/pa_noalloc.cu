@@ -52,6 +52,12 @@ PA_EXPORT pa_status pa_decode_noalloc(const pa_params* p, const void* q, const v
     int32_t S = 0, split_tokens = 0;
     pa_status st = pa_decode_plan(p, &S, &split_tokens);
     if (st != PA_OK) return st;
+    // Everything the host can check is checked before the partial step is
+    // enqueued: the output pointer (the partial step does not see it) and the
+    // options the fixed split plan does not take.
+    if (!out) return PA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(out) & 15u) return PA_ERR_ALIGN;
+    if (p->decode_q_rows > 1 || p->sliding_window > 0 || p->head_dim == 256) return PA_ERR_UNSUPPORTED;
     // partial layout: m/l pairs, then the 256-byte aligned accumulators
     const size_t n = size_t(p->num_seqs) * p->num_q_heads * S;
     const size_t acc_off = round256(n * 2 * sizeof(float));

@@ -2,7 +2,7 @@
 // 5th-generation tensor cores (tcgen05 MMA, accumulators in tensor memory,
 // operands staged by TMA).
 //
-// One CTA per (row tile, kv head, sequence).  The MMA tile's 128 rows are
+// One CTA per (row-tile pair, kv head, sequence).  The MMA tile's 128 rows are
 // the query heads of one kv head times 128/G consecutive chunk rows
 // (row = token * G + head), so every K/V tile in shared memory serves all
 // G heads (minfer doc 71: the GQA-batched shape; crucible results: K/V is
@@ -65,7 +65,6 @@ constexpr uint32_t kVOff = kKOff + kKS * kTileBytes;
 constexpr uint32_t kBarOff = kVOff + kVS * kTileBytes;
 constexpr uint32_t kNumBars = 1 + 2 * kKS + 2 * kVS + 2 * 3 + 1;
 constexpr uint32_t kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
-constexpr uint32_t kWaitLimit = 1u << 22;     // polls, for the final drains
 constexpr uint64_t kWaitNs = 2000000000ull;     // a role gives up after 2 s on one barrier
 constexpr uint32_t kSleepNs = 20000;            // longest sleep inside one try_wait
 constexpr float kRescaleStep = 8.f;  // raise the running max only when it grows by > 2^8
@@ -82,6 +81,7 @@ struct TcParams {
     float* out;
     uint32_t* dev_status;
     int32_t Hq, Hkv, G, tq, P, num_pages, max_blocks, max_q_len, total_q;
+    int32_t n_pairs;  // row-tile pairs per (sequence, kv head)
     int32_t head_first;
     float scale_log2;  // > 0
 };
@@ -153,8 +153,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const TcParams a) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    const int g = blockIdx.x % a.Hkv, b = blockIdx.x / a.Hkv;
-    const int pair = gridDim.y - 1 - blockIdx.y;  // heaviest row tiles first
+    // The row-tile pairs of one (sequence, kv head) are consecutive CTAs, so
+    // they run at the same time and read its K/V tiles through L2 from one
+    // DRAM read; within a group the heaviest pairs come first.
+    const int gb = blockIdx.x / a.n_pairs;
+    const int g = gb % a.Hkv, b = gb / a.Hkv;
+    const int pair = a.n_pairs - 1 - int(blockIdx.x % a.n_pairs);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = a.G, P = a.P, tq = a.tq;
 
@@ -290,9 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             if (!ok) raise_abort(abort_flag, a.dev_status);
             // never leave the CTA with copies in flight
-            for (int j = max(0, kq - kKS); j < kq; ++j) mbar_wait(&k_full[j % kKS], (j / kKS) & 1, kWaitLimit);
-            for (int j = max(0, vq - kVS); j < vq; ++j) mbar_wait(&v_full[j % kVS], (j / kVS) & 1, kWaitLimit);
-            if (!mbar_wait(q_full, 0, kWaitLimit)) flag(a.dev_status, PA_DEV_TIMEOUT);
+            for (int j = max(0, kq - kKS); j < kq; ++j) mbar_wait_ns(&k_full[j % kKS], (j / kKS) & 1, kWaitNs);
+            for (int j = max(0, vq - kVS); j < vq; ++j) mbar_wait_ns(&v_full[j % kVS], (j / kVS) & 1, kWaitNs);
+            if (!mbar_wait_ns(q_full, 0, kWaitNs)) flag(a.dev_status, PA_DEV_TIMEOUT);
         }
     } else if (warp == kMmaWarp) {
         // ================================== MMA ===================================
@@ -363,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) raise_abort(abort_flag, a.dev_status);
             // every MMA issued so far has finished before tensor memory is freed
             tc::commit(mma_done);
-            if (!mbar_wait(mma_done, 0, kWaitLimit)) flag(a.dev_status, PA_DEV_TIMEOUT);
+            if (!mbar_wait_ns(mma_done, 0, kWaitNs)) flag(a.dev_status, PA_DEV_TIMEOUT);
         }
     } else if (warp < 4 || has_b) {
         // ================================= softmax =================================
@@ -553,7 +557,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 template <typename T>
 cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& p,
-                         int n_tiles, int B, cudaStream_t st) {
+                         int n_ctas, cudaStream_t st) {
     auto kern = prefill_tc<T>;
     static bool configured = false;  // benign race: every caller sets the same value
     if (!configured) {
@@ -561,7 +565,7 @@ cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<dim3(p.Hkv * B, n_tiles), kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+    kern<<<dim3(n_ctas), kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 
@@ -639,10 +643,12 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cuda
     p.total_q = a.total_q;
     p.head_first = head_first;
     p.scale_log2 = a.scale_log2;
-    const int n_tiles = (a.max_q_len + 2 * tq - 1) / (2 * tq);  // pairs of row tiles
-    if (n_tiles > 65535 || int64_t(a.num_kv_heads) * a.num_seqs > 0x7fffffff) return cudaErrorInvalidValue;
-    return dt == PA_BF16 ? launch_typed<__nv_bfloat16>(mq, mk, mv, p, n_tiles, a.num_seqs, st)
-                         : launch_typed<__half>(mq, mk, mv, p, n_tiles, a.num_seqs, st);
+    const int64_t n_pairs = (a.max_q_len + 2 * tq - 1) / (2 * tq);  // pairs of row tiles
+    const int64_t n_ctas = n_pairs * a.num_kv_heads * a.num_seqs;
+    if (n_ctas > 0x7fffffff) return cudaErrorInvalidValue;
+    p.n_pairs = int32_t(n_pairs);
+    return dt == PA_BF16 ? launch_typed<__nv_bfloat16>(mq, mk, mv, p, int(n_ctas), st)
+                         : launch_typed<__half>(mq, mk, mv, p, int(n_ctas), st);
 }
 
 }  // namespace pa

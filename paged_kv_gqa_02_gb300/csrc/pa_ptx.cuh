@@ -63,12 +63,17 @@ __device__ inline uint64_t globaltimer_ns() {
     return t;
 }
 
-// Waits for the phase with the given parity; gives up after `limit` polls
-// (each poll may suspend the thread for a short hardware-chosen time).
-__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i)
+// Waits for the phase with the given parity; gives up once `limit_ns`
+// nanoseconds of the global timer have passed (each poll may suspend the
+// thread for a short hardware-chosen time), so the bound holds however slow
+// the copies behind the barrier are.
+__device__ inline bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-    return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
 }
 
 // Orders this thread's generic-proxy shared-memory accesses before later

@@ -73,8 +73,9 @@ def load(path: str = LIB_PATH):
             L.pa_prefill_workspace_size.argtypes = [P, i32, i32]
             L.pa_prefill_workspace_size.restype = sz
             L.pa_prefill_chunk.argtypes = [P, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+            L.pa_decode_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
             for name in ("pa_decode_plan", "pa_decode", "pa_decode_append", "pa_decode_partial",
-                         "pa_combine", "pa_prefill_chunk"):
+                         "pa_combine", "pa_prefill_chunk", "pa_decode_noalloc"):
                 getattr(L, name).restype = ctypes.c_int
             L.pa_version.restype = i32
             _lib = L
@@ -243,12 +244,7 @@ def decode_noalloc(p: Params, q, k_cache, v_cache, block_tables, context_lens, o
     """pa_decode_noalloc: decode with the split partials in the library's
     static device scratch (for callers that cannot allocate at call time).
     Raises PaError(PA_ERR_WORKSPACE) when the partials exceed the scratch."""
-    L = load()
-    fn = L.pa_decode_noalloc
-    if fn.restype is not ctypes.c_int:
-        vp = ctypes.c_void_p
-        fn.argtypes = [ctypes.POINTER(Params), vp, vp, vp, vp, vp, vp, vp, vp]
-        fn.restype = ctypes.c_int
+    fn = load().pa_decode_noalloc
     if out is None:
         out = _empty_out(q, p)
     _check(fn(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),

@@ -150,25 +150,19 @@ def test_decode_workload_full(wl):
     assert_within(got, ref, wl.tol, wl.name)
 
 
-def test_prefill_workload_sampled():
-    """The 8 x (2048 + 512) prefill at full size, checked on sampled rows
-    (first, last and random rows of every chunk; every head group)."""
+def test_prefill_workload_full():
+    """The 8 x (2048 + 512) prefill at full size, compared with the oracle
+    element by element: all 4,096 rows x 64 q heads x 128 dims (the oracle
+    takes about 1.5e11 fp64 multiply-adds, spread over the host's cores)."""
     wl = workloads.C5
     inp = wl.make_inputs()
     meta = dict(num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
                 page_size=wl.page_size, scale=wl.scale, q_dtype=wl.q_dtype, kv_dtype=wl.kv_dtype)
     got, status = gpu_prefill(inp, meta)
     assert status == 0
-    rng = np.random.default_rng(5)
-    picks = []
-    for s in range(wl.num_seqs):
-        base = s * 512
-        for r in (0, 1, 255, 510, 511, int(rng.integers(2, 510))):
-            picks.append((base + r, int(rng.integers(0, wl.num_q_heads))))
-    ref = oracle.attention_rows(inp, picks, wl)
-    sel = np.stack([got[r, h] for r, h in picks])
-    assert_within(sel, ref, wl.tol, "prefill C5 sampled")
-    assert np.isfinite(got).all()
+    assert got.shape == (wl.total_q, wl.num_q_heads, wl.head_dim)
+    ref = oracle.attention(inp, wl, threads=max(1, os.cpu_count() or 1))
+    assert_within(got, ref, wl.tol, "prefill C5 full")
 
 
 # ------------------------------------------------------ partial / combine --
