@@ -293,21 +293,39 @@ def time_graph(torch, calls, K, W, world):
     return e0.elapsed_time(e1), t0, t1
 
 
-def decode_calls(rot, ops, torch, partial_only=False):
+def decode_calls(rot, ops, torch, partial_only=False, single=False):
     """pa_decode calls over the rotation copies; with partial_only, the same
-    calls restricted to the partial kernel (decode_phases = 1)."""
+    calls restricted to the partial kernel (decode_phases = 1); with single,
+    the single-launch form (single_launch = 1)."""
     import copy
     p = copy.copy(rot.params)
     p.decode_phases = 1 if partial_only else 0
+    p.single_launch = 1 if single and not partial_only else 0
     S, _ = ops.decode_plan(p)
     nws = ops.decode_workspace_size(p)
-    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device="cuda")
     calls = [lambda s, i=i: ops.decode(p, rot.q[i], rot.k, rot.v, rot.bt[i], rot.cl, out=rot.out,
                                        workspace=ws if nws else None, stream=s)
              for i in range(rot.R)]
-    two_kernels = p.num_splits == 0 and p.kv_dtype != ops.PA_F32 or S > 1
-    launches = 1 if partial_only or not two_kernels else 2
+    if partial_only:
+        launches = 1
+    elif p.num_splits == 0 and p.kv_dtype != ops.PA_F32:
+        launches = 1 if single_launch(p) else 2
+    else:
+        launches = 2 if S > 1 else 1
     return calls, launches, S
+
+
+def single_launch(p) -> bool:
+    """Whether pa_decode runs these parameters as one kernel: single_launch
+    asked for, 16-bit K/V, automatic splits, head_dim <= 128 and one MMA
+    column tile (query rows x q heads per kv head <= 8)."""
+    from paged_kv_gqa_02_gb300 import ops
+    rows = max(1, p.decode_q_rows)
+    g = p.num_q_heads // p.num_kv_heads
+    rb = min(rows, (8 if p.head_dim == 256 else 16) // g)
+    return (p.single_launch == 1 and p.num_splits == 0 and p.kv_dtype != ops.PA_F32
+            and p.head_dim <= 128 and rb * g <= 8 and p.decode_phases in (0, 3))
 
 
 def append_calls(rot, wl, ops, torch):
@@ -319,7 +337,7 @@ def append_calls(rot, wl, ops, torch):
     kn, vn = ops.to_device(k_new, wl.kv_dtype), ops.to_device(v_new, wl.kv_dtype)
     p = rot.params
     nws = ops.decode_workspace_size(p)
-    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device="cuda")
     return [lambda s, i=i: ops.decode_append(p, rot.q[i], kn, vn, rot.k, rot.v, rot.bt[i], rot.cl, out=rot.out,
                                              workspace=ws if nws else None, stream=s)
             for i in range(rot.R)]
@@ -337,7 +355,7 @@ def rows_calls(rot, wl, ops, torch, T):
     cl = torch.clamp(rot.cl, min=T)
     out = torch.empty((wl.num_seqs * T, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
     nws = ops.decode_workspace_size(p)
-    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device="cuda")
     return [lambda s, i=i: ops.decode(p, q, rot.k, rot.v, rot.bt[i], cl, out=out,
                                       workspace=ws if nws else None, stream=s)
             for i in range(rot.R)]
@@ -349,7 +367,7 @@ def window_calls(rot, wl, ops, torch, W):
     p = copy.copy(rot.params)
     p.sliding_window = W
     nws = ops.decode_workspace_size(p)
-    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device="cuda")
     return [lambda s, i=i: ops.decode(p, rot.q[i], rot.k, rot.v, rot.bt[i], rot.cl, out=rot.out,
                                       workspace=ws if nws else None, stream=s)
             for i in range(rot.R)]
@@ -377,7 +395,7 @@ def e2e_decode(wl, inp, ops, torch, steps):
     out_d = torch.empty((wl.total_q, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
     out_h = torch.empty_like(out_d, device="cpu").pin_memory()
     nws = ops.decode_workspace_size(p)
-    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device="cuda")
     s = torch.cuda.Stream()
 
     def step():
@@ -500,13 +518,24 @@ def measure_workload(wl, ops, torch, K, W, world, l2, hbm_peak, flop_peak, clock
         calls, launches, S = decode_calls(rot, ops, torch)
         ms, t0, t1 = time_graph(torch, calls, K, W, world)
         ms = max_over_ranks(ms, world)
+        # the partial step alone (decode_phases = 1: the split partial kernel
+        # of the two-kernel form)
         pcalls, _, _ = decode_calls(rot, ops, torch, partial_only=True)
         pms, _, _ = time_graph(torch, pcalls, K, W, world)
         pms = max_over_ranks(pms, world)
         per_call = ms / K
         part = pms / K
-        dom_bytes = wl.kv_bytes() + wl.q_bytes()
-        achieved = dom_bytes / (part * 1e-3) / 1e9
+        if launches == 1:
+            # one kernel per call: its average launch period is the call's,
+            # and it moves every algorithmic byte (K/V, q and out)
+            dom_name, dom_ms, dom_bytes = "decode (single launch)", per_call, wl.algorithmic_bytes()
+        else:
+            dom_name, dom_ms, dom_bytes = "decode split partial", part, wl.kv_bytes() + wl.q_bytes()
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+        scalls, slaunches, _ = decode_calls(rot, ops, torch, single=True)
+        if slaunches == 1:
+            sms, _, _ = time_graph(torch, scalls, K, W, world)
+            res["single_launch_us_per_call"] = max_over_ranks(sms, world) / K * 1e3
         ams, _, _ = time_graph(torch, append_calls(rot, wl, ops, torch), K, W, world)
         res["append_us_per_call"] = max_over_ranks(ams, world) / K * 1e3
         for T in (2, 4):
@@ -521,7 +550,8 @@ def measure_workload(wl, ops, torch, K, W, world, l2, hbm_peak, flop_peak, clock
         res.update(num_splits=S, launches_per_call=launches, ms_total=ms, us_per_call=per_call * 1e3,
                    gbs=wl.algorithmic_bytes() / (per_call * 1e-3) / 1e9,
                    frac_of_hbm=wl.algorithmic_bytes() / (per_call * 1e-3) / 1e9 / hbm_peak,
-                   dominant={"kernel": "decode_partial", "us_per_launch": part * 1e3,
+                   partial_only_us=part * 1e3,
+                   dominant={"kernel": dom_name, "us_per_launch": dom_ms * 1e3,
                              "algorithmic_bytes": dom_bytes, "achieved_gbs": achieved,
                              "frac": achieved / hbm_peak}, t0=t0, t1=t1)
     else:
@@ -580,12 +610,13 @@ def run_ours(args):
     value = wl.algorithmic_bytes() * K * world / (main["ms_total"] * 1e-3) / 1e9
     dom = main.get("dominant")
     if dom:
-        traffic = read_traffic(wl.name, "decode_partial")
+        traffic = read_traffic(wl.name, "decode_v1")
         roof = {"bound": "hbm", "achieved": round(dom["achieved_gbs"], 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(dom["achieved_gbs"] / hbm, 4),
                 "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs, copy)",
-                "kernel": "decode split partial", "us_per_launch": round(dom["us_per_launch"], 3),
-                "algorithmic_bytes_per_launch": dom["algorithmic_bytes"]}
+                "kernel": dom["kernel"], "us_per_launch": round(dom["us_per_launch"], 3),
+                "algorithmic_bytes_per_launch": dom["algorithmic_bytes"],
+                "partial_step_alone_us": round(main["partial_only_us"], 3)}
     else:
         roof = {"bound": "tensor", "achieved": round(main["tflops"], 1), "peak": bf16,
                 "unit": "TFLOP/s", "frac": round(main["tflops"] / bf16, 4),
@@ -608,6 +639,8 @@ def run_ours(args):
                    "timing": "CUDA graph replays, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
         "decode_append_us_per_call": round(main["append_us_per_call"], 3) if "append_us_per_call" in main else None,
+        "decode_single_launch_us_per_call": round(main["single_launch_us_per_call"], 3)
+        if "single_launch_us_per_call" in main else None,
         "decode_rows_us_per_call": {T: round(main[f"rows{T}_us_per_call"], 3) for T in (2, 4)
                                     if f"rows{T}_us_per_call" in main},
         "decode_window1024": {"us_per_call": round(main["window1024_us_per_call"], 3),

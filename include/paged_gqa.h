@@ -80,6 +80,10 @@ typedef enum {
 #define PA_DEV_BAD_PAGE 1u /* a block-table entry outside [0, num_pages) */
 #define PA_DEV_BAD_LEN 2u  /* context_len < T_s or > max_blocks_per_seq * page_size */
 #define PA_DEV_TIMEOUT 4u  /* a bounded device wait gave up */
+/* Library built with PA_CHECKED defined only: a computed global index left
+ * its buffer (block table, lengths, q, out, workspace); the access was
+ * skipped.  A release build never sets it. */
+#define PA_DEV_OOB 8u
 
 typedef struct {
     int32_t num_seqs;           /* B                                           */
@@ -100,10 +104,15 @@ typedef struct {
     pa_dtype out_dtype;         /* PA_F32                                      */
     int32_t deterministic;      /* 1: split plan from pa_params alone           */
     int32_t num_splits;         /* decode: 0 = automatic, else requested count  */
-    int32_t decode_phases;      /* pa_decode: 0 = both steps; 1 = partial step
-                                   only; 2 = combine step only (after a
-                                   phase-1 call on the same workspace, to put
-                                   other work between the two or time them)     */
+    int32_t decode_phases;      /* pa_decode: 0 = the whole call (one kernel
+                                   when the call takes the single-launch form
+                                   below); 1 = partial step only; 2 = combine
+                                   step only (after a phase-1 call on the same
+                                   workspace, to put other work between the two
+                                   or time them).  1 then 2 is the two-kernel
+                                   form: equal to the whole call within the
+                                   decode tolerances (bit for bit where the
+                                   call has no single-launch form)             */
     int32_t decode_q_rows;      /* pa_decode: query rows per sequence, 0 or 1 =
                                    one; up to 16 (speculative / multi-token
                                    decode).  q and out are then [B][rows][Hq][D]
@@ -130,6 +139,13 @@ typedef struct {
                                    pa_decode_append with 16-bit K/V and
                                    automatic splits only; otherwise
                                    PA_ERR_UNSUPPORTED.                            */
+    int32_t single_launch;      /* pa_decode / pa_decode_append: 1 = run the
+                                   call as one kernel where it can (16-bit K/V,
+                                   automatic splits, head_dim <= 128, rows x
+                                   Hq/Hkv <= 8): the split partial kernel also
+                                   merges the pieces (see pa_decode).  0 (the
+                                   default) = partial kernel + combine kernel,
+                                   the faster form on GB300.                     */
 } pa_params;
 
 /* Fills *p with defaults: contiguous strides, PA_F32 out, automatic splits,
@@ -161,7 +177,12 @@ size_t pa_decode_workspace_size(const pa_params *p);
 
 /* Decode attention: the split partials and their combine.
  * workspace: device memory of at least pa_decode_workspace_size(p) bytes,
- * 256-byte aligned, contents ignored.  dev_status may be NULL.
+ * 256-byte aligned.  Its first PA_DECODE_COUNTER_BYTES bytes hold arrival
+ * counters: they must be zero before the first pa_decode or
+ * pa_decode_append call that uses the buffer (zero the whole buffer once
+ * after allocating it, e.g. with cudaMemsetAsync), and every call leaves
+ * them zero, whatever its parameters, so a buffer is zeroed once.  The
+ * other bytes are scratch: contents ignored.  dev_status may be NULL.
  *
  * With num_splits = 0 and 16-bit K/V the partition is length-balanced: one
  * persistent CTA per SM (a fixed 152 when deterministic = 1, the device's
@@ -169,9 +190,22 @@ size_t pa_decode_workspace_size(const pa_params *p);
  * ordered (sequence, kv head [, row block], page) list, and its warps split
  * the share the same way (fewer warps for small calls when the group needs
  * two MMA column tiles or head_dim is 256); units that fall inside one
- * share are finished there, and a second kernel merges the pieces of the
- * others in ascending share order.  Otherwise the fixed split
- * plan of pa_decode_plan is used (the pa_decode_partial + pa_combine pair). */
+ * share are finished there.  The pieces of the others are merged in
+ * ascending share order:
+ *  - by a second kernel, launched with programmatic dependent launch so that
+ *    its CTAs are resident and have located their pieces when the partial
+ *    kernel ends (the default);
+ *  - with single_launch = 1, head_dim <= 128 and rows x Hq/Hkv <= 8 (one MMA
+ *    column tile), in the partial kernel itself: each CTA merges its warps'
+ *    pieces, and the last CTA to leave a piece of a unit (counted on a
+ *    workspace counter with an acquire-release atomic) merges the unit's CTA
+ *    pieces.  One kernel per call; on GB300 it takes longer than the pair,
+ *    because the count and the finishing CTA's reads sit on the critical
+ *    path after the slowest CTA.
+ * Otherwise the fixed split plan of pa_decode_plan is used (the
+ * pa_decode_partial + pa_combine pair). */
+#define PA_DECODE_COUNTER_BYTES 4096u
+
 pa_status pa_decode(const pa_params *p, const void *q, const void *k_cache,
                     const void *v_cache, const int32_t *block_tables,
                     const int32_t *context_lens, float *out, void *workspace,
@@ -219,13 +253,20 @@ pa_status pa_decode_partial(const pa_params *p, const void *q, const void *k_cac
                             uint32_t *dev_status, pa_stream_t stream);
 
 /* Combine (crucible README "Split-position attention": rescale each split
- * by exp(m_i - m_max) and merge; minfer doc 71 Excerpt F: empty splits get
- * weight zero).  For each (b, h), in ascending split order:
+ * by exp(m_i - m_max) and merge; minfer doc 71 Excerpt F: idle splits write
+ * m = -inf and get weight zero).  partial_ml is [B][Hq][max_splits][2] and
+ * partial_acc [B][Hq][max_splits][D] (the layout pa_decode_partial writes).
+ * For each (b, h), over splits i < S_b in ascending order:
  *   M = max_i m_i;  w_i = 2^(m_i - M) (0 when m_i = -inf);
  *   out[b][h][:] = sum_i w_i acc_i / sum_i w_i l_i,  or 0 when every m_i = -inf.
- * Uses p->num_seqs, num_q_heads, head_dim; out is [B][Hq][D] f32. */
+ * S_b = splits_per_seq[b] clamped to [0, max_splits] when splits_per_seq
+ * (device memory, [B] int32) is non-NULL, else max_splits; splits at or
+ * past S_b are never read (S_b = 0 writes zeros).
+ * Uses p->num_seqs, num_q_heads, head_dim; out is [B][Hq][D] f32.
+ * partial_acc and out 16-byte aligned, partial_ml 8-byte aligned. */
 pa_status pa_combine(const pa_params *p, const float *partial_ml, const float *partial_acc,
-                     int32_t num_splits, float *out, pa_stream_t stream);
+                     int32_t max_splits, const int32_t *splits_per_seq, float *out,
+                     pa_stream_t stream);
 
 /* Decode without a workspace argument (the pages have no counterpart: this
  * entry point exists for callers that cannot allocate device memory at call
@@ -283,6 +324,11 @@ pa_status pa_prefill_chunk(const pa_params *p, const void *q, const int32_t *cu_
 
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t pa_version(void);
+
+/* How this library was built: PA_BUILD_CHECKED when PA_CHECKED was defined
+ * (kernels range-check their computed global indices; see PA_DEV_OOB). */
+#define PA_BUILD_CHECKED 1
+int32_t pa_build_flags(void);
 
 #ifdef __cplusplus
 }

@@ -2,7 +2,10 @@
 
 Each ``csrc/*.cu`` translation unit is compiled in parallel, then linked
 into one shared library with the CUDA runtime linked statically and only the
-``pa_*`` entry points exported.
+``pa_*`` entry points exported.  ``build(checked=True)`` builds the same
+sources with PA_CHECKED defined into libpaged_gqa_checked.so: every kernel
+range-checks its computed global indices and reports a violation through
+PA_DEV_OOB instead of making the access.
 """
 from __future__ import annotations
 
@@ -19,6 +22,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpaged_gqa.so")
+CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
+CHECKED_LIB = os.path.join(PKG, "libpaged_gqa_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,26 +43,28 @@ def _deps():
         os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "paged_gqa.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), checked: bool = False) -> str:
+    lib = CHECKED_LIB if checked else LIB
+    build_dir = CHECKED_BUILD_DIR if checked else BUILD_DIR
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-I", INCLUDE, "-I", CSRC,
                     "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr",
-                    *extra]
+                    *(["-DPA_CHECKED"] if checked else []), *extra]
     if verbose:
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         r = subprocess.run([cc, *flags, "-c", src, "-o", obj], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -68,14 +75,14 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-cudart", "static", "-Xlinker", "--exclude-libs,ALL",
                         *objs, "-o", tmp], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

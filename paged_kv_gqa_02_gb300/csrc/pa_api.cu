@@ -51,6 +51,7 @@ pa_status check_params(const pa_params* p, Resolved* r) {
     if (p->decode_q_rows < 0 || p->decode_q_rows > kMaxDecodeRows) return PA_ERR_SHAPE;
     if (p->decode_q_rows > p->max_context_len) return PA_ERR_SHAPE;
     if (p->sliding_window < 0) return PA_ERR_SHAPE;
+    if (p->single_launch != 0 && p->single_launch != 1) return PA_ERR_SHAPE;
     const int64_t D = p->head_dim;
     r->head_stride = p->head_stride ? p->head_stride : D;
     r->token_stride = p->token_stride ? p->token_stride : p->num_kv_heads * r->head_stride;
@@ -141,9 +142,12 @@ int row_blocks(const pa_params* p) { return (decode_rows(p) + row_block(p) - 1) 
 int v1_ctas(const pa_params* p) { return p->deterministic ? kRefSms : device_sms(); }
 
 // Split partials of every (row, q head): rows = query rows per sequence.
-size_t partial_bytes(const pa_params* p, int S, size_t* acc_off, int rows = 1) {
+// They start after the counter block that pa_decode's single launch keeps at
+// the head of every decode workspace, so one zeroed buffer serves both paths.
+size_t partial_bytes(const pa_params* p, int S, size_t* ml_off, size_t* acc_off, int rows = 1) {
     const size_t n = size_t(p->num_seqs) * rows * p->num_q_heads * S;
-    *acc_off = align256(n * 2 * sizeof(float));
+    *ml_off = PA_DECODE_COUNTER_BYTES;
+    *acc_off = *ml_off + align256(n * 2 * sizeof(float));
     return *acc_off + align256(n * p->head_dim * sizeof(float));
 }
 
@@ -197,7 +201,15 @@ PA_EXPORT const char* pa_status_string(pa_status s) {
     return "unknown pa_status";
 }
 
-PA_EXPORT int32_t pa_version(void) { return 100; }
+PA_EXPORT int32_t pa_version(void) { return 200; }
+
+PA_EXPORT int32_t pa_build_flags(void) {
+#ifdef PA_CHECKED
+    return PA_BUILD_CHECKED;
+#else
+    return 0;
+#endif
+}
 
 PA_EXPORT pa_status pa_decode_plan(const pa_params* p, int32_t* num_splits, int32_t* split_tokens) {
     Resolved r;
@@ -221,8 +233,8 @@ PA_EXPORT size_t pa_decode_workspace_size(const pa_params* p) {
     int S, tok;
     plan(p, &S, &tok);
     if (S == 1 || !rows_split_ok(p)) return 0;
-    size_t off;
-    return partial_bytes(p, S, &off, decode_rows(p));
+    size_t ml_off, acc_off;
+    return partial_bytes(p, S, &ml_off, &acc_off, decode_rows(p));
 }
 
 PA_EXPORT pa_status pa_decode_partial(const pa_params* p, const void* q, const void* k_cache,
@@ -250,15 +262,20 @@ PA_EXPORT pa_status pa_decode_partial(const pa_params* p, const void* q, const v
 }
 
 PA_EXPORT pa_status pa_combine(const pa_params* p, const float* partial_ml,
-                               const float* partial_acc, int32_t num_splits, float* out,
-                               pa_stream_t stream) {
+                               const float* partial_acc, int32_t max_splits,
+                               const int32_t* splits_per_seq, float* out, pa_stream_t stream) {
     if (!p || !partial_ml || !partial_acc || !out) return PA_ERR_NULL;
-    if (p->num_seqs < 1 || p->num_q_heads < 1 || num_splits < 1 || p->num_seqs > 65535)
+    if (p->num_seqs < 1 || p->num_q_heads < 1 || max_splits < 1 || p->num_seqs > 65535 ||
+        p->num_q_heads > 65535)
         return PA_ERR_SHAPE;
     if (p->head_dim == 256) return PA_ERR_UNSUPPORTED;
     if (p->head_dim != 64 && p->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(partial_acc) || !aligned16(out) || (reinterpret_cast<uintptr_t>(partial_ml) & 7u) ||
+        (reinterpret_cast<uintptr_t>(splits_per_seq) & 3u))
+        return PA_ERR_ALIGN;
     return cuda_status(pa::launch_combine_v0(partial_ml, partial_acc, out, p->num_seqs,
-                                             p->num_q_heads, num_splits, p->head_dim, stream));
+                                             p->num_q_heads, max_splits, p->head_dim, stream,
+                                             splits_per_seq));
 }
 
 namespace {
@@ -313,6 +330,7 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         c.row0 = 0;
         c.row_count = rows;
         c.row_block = rb;  // blocks of rows are units of one launch
+        c.single_launch = p->single_launch;
         return cuda_status(pa::launch_decode_v1(c, stream));
     }
     if (p->sliding_window > 0) return PA_ERR_UNSUPPORTED;  // windows: split-KV kernel only
@@ -333,12 +351,12 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
             if (!(phases & 1)) return PA_OK;
             return cuda_status(pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
         }
-        size_t acc_off;
-        const size_t need = partial_bytes(p, S, &acc_off, rows);
+        size_t ml_off, acc_off;
+        const size_t need = partial_bytes(p, S, &ml_off, &acc_off, rows);
         if (!workspace) return PA_ERR_NULL;
         if (workspace_bytes < need) return PA_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_ALIGN;
-        a.partial_ml = static_cast<float*>(workspace);
+        a.partial_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
         a.partial_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_off);
         if (phases & 1) {
             cudaError_t e = pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream);
@@ -364,12 +382,12 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         if (!(phases & 1)) return PA_OK;
         return cuda_status(pa::launch_decode_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
     }
-    size_t acc_off;
-    const size_t need = partial_bytes(p, S, &acc_off);
+    size_t ml_off, acc_off;
+    const size_t need = partial_bytes(p, S, &ml_off, &acc_off);
     if (!workspace) return PA_ERR_NULL;
     if (workspace_bytes < need) return PA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_ALIGN;
-    a.partial_ml = static_cast<float*>(workspace);
+    a.partial_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
     a.partial_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_off);
     if (phases & 1) {
         cudaError_t e = pa::launch_decode_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream);

@@ -35,6 +35,8 @@ struct AttnArgs {
     int32_t max_q_len;    // prefill: host bound on rows per sequence
     int32_t total_q;      // rows in q / out
     int32_t rows_per_seq = 0;  // > 1 with cu_q_lens == nullptr: sequence b owns rows b*n .. b*n + n - 1
+    // Extents, in elements, for the checked build's range checks
+    int64_t q_elems = 0, out_elems = 0, partial_items = 0;
 };
 
 // ---- element conversions -------------------------------------------------
@@ -83,5 +85,21 @@ __device__ inline float warp_sum(float v) {
 __device__ inline void flag(uint32_t* status, uint32_t bit) {
     if (status) atomicOr(status, bit);
 }
+
+// Checked builds (PA_CHECKED defined): PA_IN(i, n, st) is true when the
+// computed index i lies in [0, n); otherwise it sets PA_DEV_OOB in *st and is
+// false, so the guarded access is skipped.  Release builds compile it to
+// `true`: the kernels' index arithmetic keeps every access in range by
+// construction, and the checked build is how that is tested.
+#ifdef PA_CHECKED
+__device__ inline bool checked_in(long long i, long long n, uint32_t* status) {
+    if (i >= 0 && i < n) return true;
+    flag(status, PA_DEV_OOB);
+    return false;
+}
+#define PA_IN(i, n, st) (::pa::checked_in((long long)(i), (long long)(n), (st)))
+#else
+#define PA_IN(i, n, st) (true)
+#endif
 
 }  // namespace pa

@@ -53,6 +53,10 @@ constexpr int kSmemLimit = 232448;            // 227 KiB opt-in per CTA
 constexpr int kUnitCost = 2;                  // partition weight of a unit piece, in pages
 constexpr int kMinCtaCost = 3;                // smallest share worth a CTA, in cost units
 constexpr int kCtaMergeMaxShare = 16;         // CTA merge only while CTA shares average at most this
+// Single launch: a unit split over CTAs c0 .. c1 counts its pieces on counter
+// c0 (each CTA boundary is crossed by at most one unit), so the counters take
+// a fixed block at the start of the workspace whatever the call's sizes.
+constexpr int kMaxCounters = int(PA_DECODE_COUNTER_BYTES / sizeof(unsigned));
 
 struct V1Params {
     const void* q;  // [B*Hq][D]
@@ -61,6 +65,9 @@ struct V1Params {
     float* out;
     float* ws_ml;   // [slot][G][2]
     float* ws_acc;  // [slot][G][D]
+    unsigned* ws_cnt;  // [kMaxCounters] arrival counters, zero between calls
+    long long ws_slots;               // pieces the workspace holds
+    long long q_rows, out_rows;       // [B][T][Hq] rows of D in q and out (this launch's T)
     uint32_t* dev_status;
     int32_t B, Hq, Hkv, G, num_pages, max_blocks, max_len;
     int32_t window;     // > 0: a row sees only its last `window` keys
@@ -74,6 +81,11 @@ struct V1Params {
     float scale_log2;
     int32_t n_ctas, ntiles, head_first, unit_cost;
     int32_t cta_pieces;  // 1: the group fits one MMA column tile, so small calls merge per CTA
+    // 1: single launch (asked for by the caller).  Every call merges its
+    // warps' pieces per CTA, and the last CTA to leave a piece of a unit
+    // merges that unit's CTA pieces, so no combine kernel runs (one column
+    // tile, head_dim <= 128 only)
+    int32_t finish;
     // KV append (nullptr: none): the new token of sequence b, kv head g is
     // row L_b - 1 of the cache; it is written there and used in place of the
     // row the page copy brought in
@@ -91,7 +103,7 @@ template <int D, int P>
 __device__ inline void append_row(uint8_t* tile, const void* src_all, void* cache, const V1Params& a, int b,
                                   int g, int pg, int row) {
     const int lane = threadIdx.x & 31;
-    if (lane < D / 8) {
+    if (lane < D / 8 && PA_IN((long long)b * a.Hkv + g, (long long)a.B * a.Hkv, a.dev_status)) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src_all) +
                                                              ((long long)b * a.Hkv + g) * D) +
                               lane);
@@ -127,7 +139,7 @@ __device__ inline int unit_cols(const V1Params& a, int u) {
 // Pages of sequence b that the unit reads (0: invalid length, fewer keys
 // than query rows): from first_page to the page of key L - 1.
 __device__ inline int seq_pages(const V1Params& a, int b, int P) {
-    const int L = __ldg(a.context_lens + b);
+    const int L = PA_IN(b, a.B, a.dev_status) ? __ldg(a.context_lens + b) : 0;
     const int n = pages_of_len(L, P, a.max_len, a.T);
     return n > 0 ? n - first_page(a, L, P) : 0;
 }
@@ -286,6 +298,63 @@ __device__ inline int warps_in_use(long long T, long long n_cta) {
     return int(w < 1 ? 1 : (w > kCW ? kCW : w));
 }
 
+// Single launch: merges the np CTA pieces of unit u (slots c0 + u ..
+// c0 + np - 1 + u, written by other CTAs of this grid) into the final rows,
+// rescaling each by 2^(m_i - M) and summing in ascending CTA order.  Every
+// thread of the CTA takes (head, 4 dims) items; the pieces are read through
+// L2 (ld.global.cg) in batches whose loads are all in flight together.
+template <int D>
+__device__ inline void finish_unit(const V1Params& a, int u, int c0, int np) {
+    constexpr int kB = 16;  // pieces loaded together
+    const int G = a.G, ub = u / a.Hv, ug = u % a.Hv, Gu = unit_cols(a, ug);
+    for (int idx = threadIdx.x; idx < G * D / 4; idx += kThreadsV1) {
+        const int h = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
+        float M = -INFINITY, den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < np; j0 += kB) {
+            float2 ml[kB];
+            float4 v[kB];
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                if (j0 + j < np && PA_IN((long long)c0 + j0 + j + u, a.ws_slots, a.dev_status)) {
+                    const long long slot = (long long)c0 + j0 + j + u;
+                    ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (slot * G + h) * 2));
+                    v[j] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + (slot * G + h) * D + d4));
+                } else {
+                    ml[j] = make_float2(-INFINITY, 0.f);
+                    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            float Mn = M;
+#pragma unroll
+            for (int j = 0; j < kB; ++j) Mn = fmaxf(Mn, ml[j].x);
+            if (Mn == -INFINITY) continue;  // no key so far
+            const float sc = ex2(M - Mn);   // M = -inf -> 0
+            den *= sc;
+            num.x *= sc;
+            num.y *= sc;
+            num.z *= sc;
+            num.w *= sc;
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                if (ml[j].x == -INFINITY) continue;  // an empty piece: weight 0
+                const float w = ex2(ml[j].x - Mn);
+                den = fmaf(w, ml[j].y, den);
+                num.x = fmaf(w, v[j].x, num.x);
+                num.y = fmaf(w, v[j].y, num.y);
+                num.z = fmaf(w, v[j].z, num.z);
+                num.w = fmaf(w, v[j].w, num.w);
+            }
+            M = Mn;
+        }
+        if (h < Gu && PA_IN(row_off<D>(a, ub, ug, h) / D, a.out_rows, a.dev_status)) {
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            *reinterpret_cast<float4*>(a.out + row_off<D>(a, ub, ug, h) + d4) =
+                make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+        }
+    }
+}
+
 // The load side of a warp: lane l holds page base + l of the warp's share
 // (its kv head, page id and whether it exists).
 struct LoadWindow {
@@ -301,9 +370,10 @@ __device__ inline void window_fill(LoadWindow& lw, const V1Params& a, int P) {
     walk_advance(x, i, threadIdx.x & 31, a, P);
     lw.live = x.done ? 0 : 1;
     lw.g = x.g;
-    lw.page = lw.live ? __ldg(a.block_tables + (long long)x.b * a.max_blocks +
-                              first_page(a, __ldg(a.context_lens + x.b), P) + i)
-                      : -1;
+    const int fpg = lw.live ? first_page(a, __ldg(a.context_lens + x.b), P) : 0;
+    lw.page = lw.live && PA_IN(fpg + i, a.max_blocks, a.dev_status)
+                  ? __ldg(a.block_tables + (long long)x.b * a.max_blocks + fpg + i)
+                  : -1;
 }
 
 // At most 224 registers a thread: 256 x 224 leaves room on the SM for one
@@ -334,8 +404,13 @@ __global__ void __maxnreg__(224)
     uint64_t* tile_full = reinterpret_cast<uint64_t*>(tile_page + kMaxTiles);  // [kMaxTiles]
     __shared__ int s_unit[kCW][2];  // CTA merge: unit of each warp's pieces (-1: none)
     __shared__ int s_inside[kCW][2];
-    __shared__ float s_w[kCtaMerge ? 8 : 1][2 * kCW];  // CTA merge: weight of each entry, per head
-    __shared__ float s_md[kCtaMerge ? 8 : 1][2];       // CTA merge: max and denominator, per head
+    __shared__ long long s_p0[kCW][2];  // CTA merge: cost position of the unit's first page
+    __shared__ int s_pb[kCW][2];        // and its page count
+    __shared__ int4 s_run[2 * kCW];     // CTA merge: (unit, entry mask, inside, first entry) of each run
+    __shared__ int s_nruns;
+    __shared__ int2 s_fin[2 * kCW];     // single launch: (unit, first CTA) of each run this CTA completes
+    __shared__ int s_fnp[2 * kCW];      // and its CTA pieces
+    if (threadIdx.x < 2 * kCW) s_fin[threadIdx.x] = make_int2(-1, 0);
     if (lane == 0) {
         if constexpr (kCtaMerge) {  // eight rings, each warp initialises its own
             const int nh = min(a.ntiles / kCW, kMaxRing);
@@ -361,7 +436,7 @@ __global__ void __maxnreg__(224)
     // Small calls (short shares, few pages a warp) merge the warps' pieces in
     // the CTA, so the combine sees one piece per CTA; larger ones leave each
     // warp's pieces to the combine.  Uniform over the grid.
-    const bool cta_merge = kCtaMerge && cost <= (long long)kCtaMergeMaxShare * n_cta;
+    const bool cta_merge = kCtaMerge && (a.finish || cost <= (long long)kCtaMergeMaxShare * n_cta);
     // Warps that take a part: with the CTA merge compiled in, a call past it
     // has shares above 16 and all eight do.
     const int wpc = kCtaMerge ? kCW : warps_in_use(cost, n_cta);
@@ -448,12 +523,13 @@ __global__ void __maxnreg__(224)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int h = nt * 8 + g4;
-            const uint32_t* row =
-                reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.q) + row_off<D>(a, b, g, h < Gu ? h : 0));
+            const long long off = row_off<D>(a, b, g, h < Gu ? h : 0);
+            const bool in = h < Gu && PA_IN(off / D, a.q_rows, a.dev_status);
+            const uint32_t* row = reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.q) + off);
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
-                dst[nt][ks][0] = h < Gu ? __ldg(row + 8 * ks + t4) : 0u;
-                dst[nt][ks][1] = h < Gu ? __ldg(row + 8 * ks + 4 + t4) : 0u;
+                dst[nt][ks][0] = in ? __ldg(row + 8 * ks + t4) : 0u;
+                dst[nt][ks][1] = in ? __ldg(row + 8 * ks + 4 + t4) : 0u;
             }
         }
     };
@@ -468,6 +544,8 @@ __global__ void __maxnreg__(224)
     // stays in o / mrun / lrun.
     float of[kKs][4], mf[2], lf[2];
     int first_unit = -1, first_inside = 0, last_unit = -1, last_inside = 0;
+    long long first_p0 = 0, last_p0 = 0;  // cost position of the piece's unit's first page
+    int first_pb = 0, last_pb = 0;       // and its pages
     float mrun[NT][2], lrun[NT][2];
 
     while (!wk.done) {
@@ -693,7 +771,7 @@ __global__ void __maxnreg__(224)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int h = nt * 8 + 2 * t4 + j;
-                    if (h < Gu) {
+                    if (h < Gu && PA_IN(row_off<D>(a, wk.b, wk.g, h) / D, a.out_rows, a.dev_status)) {
                         float* ob = a.out + row_off<D>(a, wk.b, wk.g, h);
                         const float inv = lrun[nt][j] > 0.f ? 1.f / lrun[nt][j] : 0.f;
 #pragma unroll
@@ -710,6 +788,8 @@ __global__ void __maxnreg__(224)
                 if (!nx.done) {  // the share's first piece; later units follow
                     first_unit = unit;
                     first_inside = inside;
+                    first_p0 = p0;
+                    first_pb = wk.pb;
 #pragma unroll
                     for (int dt = 0; dt < kKs; ++dt)
 #pragma unroll
@@ -721,10 +801,12 @@ __global__ void __maxnreg__(224)
                 } else {
                     last_unit = unit;
                     last_inside = inside;
+                    last_p0 = p0;
+                    last_pb = wk.pb;
                 }
             }
         } else {
-            const long long slot = part + unit;
+            const long long slot = PA_IN(part + unit, a.ws_slots, a.dev_status) ? part + unit : -1;
             float* accp = a.ws_acc + slot * G * D;
             float* ml = a.ws_ml + slot * G * 2;
 #pragma unroll
@@ -732,7 +814,7 @@ __global__ void __maxnreg__(224)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int h = nt * 8 + 2 * t4 + j;
-                    if (h < G) {
+                    if (h < G && slot >= 0) {
 #pragma unroll
                         for (int dt = 0; dt < kKs; ++dt) {
                             accp[h * D + 16 * dt + g4] = o[dt][nt][j];
@@ -747,17 +829,13 @@ __global__ void __maxnreg__(224)
     }
     // A wait that gave up leaves half-stages [x_stop, n_issued) (at most NH)
     // possibly in flight: wait for each of them, bounded by the global timer,
-    // before the ring is reused for the merge or the CTA exits.  A copy that
-    // still has not landed keeps this warp's ring out of the merge.
-    bool ring_free = true;
-    if (timed_out) {
-        for (int y = x_stop; y < n_issued; ++y)
-            ring_free = mbar_wait_ns(&my_full[y % NH], (y / NH) & 1, kWaitNs) && ring_free;
-        ring_free = __all_sync(0xffffffffu, ring_free);
-    }
+    // before the ring is reused for the merge or the CTA exits.  (The results
+    // are already void, PA_DEV_TIMEOUT being set; the merge and the unit
+    // counters still run so that every counter is left at zero.)
+    if (timed_out)
+        for (int y = x_stop; y < n_issued; ++y) mbar_wait_ns(&my_full[y % NH], (y / NH) & 1, kWaitNs);
     __syncwarp();
     if (kCtaMerge && cta_merge) {
-        if (!ring_free) first_unit = last_unit = -1;  // nothing is staged in a ring still being written
         // Stage the non-whole pieces in this warp's own ring (its copies are
         // all consumed): piece k is [G][D + 4] accumulators (the pad puts the
         // 8 x 4 lanes of one store in 32 distinct banks) then [G] (m, l) pairs.
@@ -793,85 +871,127 @@ __global__ void __maxnreg__(224)
         if (lane == 0) {
             s_unit[warp][0] = first_unit;
             s_inside[warp][0] = first_inside;
+            s_p0[warp][0] = first_p0;
+            s_pb[warp][0] = first_pb;
             s_unit[warp][1] = last_unit;
             s_inside[warp][1] = last_inside;
+            s_p0[warp][1] = last_p0;
+            s_pb[warp][1] = last_pb;
         }
         __syncthreads();
-        // Merge, unit by unit in warp order, the pieces that warps of this CTA
-        // share; a unit whose pages all lie in this CTA's share is finished
-        // here, the others leave one piece for the combine (slot CTA + unit).
-        // Every warp reads the 16 entry descriptors (lane f and f + 16 hold
-        // entry f) and finds, with ballots, where each unit's entries start and
-        // which entries hold it.  The code stays short: it runs once per CTA
-        // and launch, so its instructions are fetched cold.
-        const int f = lane & (2 * kCW - 1);
-        const int su = s_unit[f >> 1][f & 1];
-        const uint32_t vmask = __ballot_sync(0xffffffffu, su >= 0) & 0xffffu;
-        const uint32_t lower = vmask & ((1u << f) - 1u);
-        const int pu = __shfl_sync(0xffffffffu, su, lower ? 31 - __clz(lower) : 0);
-        const uint32_t starts = __ballot_sync(0xffffffffu, su >= 0 && (lower == 0 || pu != su)) & 0xffffu;
-        auto piece = [&](int ff) {
-            return reinterpret_cast<const float*>(base + size_t(ff >> 1) * NH * kTile) + (ff & 1) * pstride;
-        };
-        for (uint32_t sm = starts; sm; sm &= sm - 1) {
-            const int e = __ffs(sm) - 1;
-            const int u = __shfl_sync(0xffffffffu, su, e);
-            const uint32_t emask = __ballot_sync(0xffffffffu, su == u) & 0xffffu;
-            const bool inside = s_inside[e >> 1][e & 1] != 0;
-            const int ub = u / a.Hv, ug = u % a.Hv;
-            // Weights: warp w takes heads 2w and 2w + 1, one lane per entry;
-            // maxima and denominators by fixed 16-lane shuffle trees.
-            if (2 * warp < G) {
-                const int h = 2 * warp + (lane >> 4);
-                const bool mine = h < G && ((emask >> f) & 1u);
-                const float mm = mine ? piece(f)[G * kRow + 2 * h] : -INFINITY;
-                const float ll = mine ? piece(f)[G * kRow + 2 * h + 1] : 0.f;
-                float M = mm;
+        // Entries f = 0 .. 15 (warp f / 2, first then last piece) are in cost
+        // order, and a unit's entries are consecutive: a run is a maximal group
+        // of valid entries of one unit.  Warp 0 lists the runs; then every
+        // thread takes (run, head, 4 dims) items and merges the run's entries in
+        // ascending order, all loads of an item in flight together.  A unit
+        // whose pages all lie in this CTA's share is finished here; the others
+        // leave one piece (slot CTA + unit).
+        if (warp == 0) {
+            const int f = lane & (2 * kCW - 1);
+            const int su = s_unit[f >> 1][f & 1];
+            const uint32_t vmask = __ballot_sync(0xffffffffu, su >= 0) & 0xffffu;
+            const uint32_t lower = vmask & ((1u << f) - 1u);
+            const int pu = __shfl_sync(0xffffffffu, su, lower ? 31 - __clz(lower) : 0);
+            const uint32_t starts = __ballot_sync(0xffffffffu, su >= 0 && (lower == 0 || pu != su)) & 0xffffu;
+            if (lane < 2 * kCW && ((starts >> f) & 1u)) {
+                const uint32_t above = starts & ~((2u << f) - 1u);
+                const int nxt = above ? __ffs(above) - 1 : 2 * kCW;
+                s_run[__popc(starts & ((1u << f) - 1u))] =
+                    make_int4(su, int(vmask & ((1u << nxt) - (1u << f))), s_inside[f >> 1][f & 1], f);
+            }
+            if (lane == 0) s_nruns = __popc(starts);
+        }
+        __syncthreads();
+        const int nruns = s_nruns;
+        const int per_run = G * (D / 4);
+        for (int it = threadIdx.x; it < nruns * per_run; it += kThreadsV1) {
+            const int r = it / per_run, rest = it - r * per_run;
+            const int h = rest / (D / 4), d4 = (rest % (D / 4)) * 4;
+            const int4 run = s_run[r];
+            const uint32_t emask = uint32_t(run.y);
+            float2 ml[2 * kCW];
+            float4 v[2 * kCW];
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-                const float w = mm != -INFINITY ? ex2(mm - M) : 0.f;
-                float den = w * ll;
+            for (int ff = 0; ff < 2 * kCW; ++ff) {
+                const float* pc = reinterpret_cast<const float*>(base + size_t(ff >> 1) * NH * kTile) +
+                                  (ff & 1) * pstride;
+                if ((emask >> ff) & 1u) {
+                    ml[ff] = *reinterpret_cast<const float2*>(pc + G * kRow + 2 * h);
+                    v[ff] = *reinterpret_cast<const float4*>(pc + h * kRow + d4);
+                } else {
+                    ml[ff] = make_float2(-INFINITY, 0.f);
+                    v[ff] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            float M = -INFINITY;
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-                if (h < G) {
-                    s_w[h][f] = w;
-                    if (f == 0) {
-                        s_md[h][0] = M;
-                        s_md[h][1] = den;
-                    }
+            for (int ff = 0; ff < 2 * kCW; ++ff) M = fmaxf(M, ml[ff].x);
+            float den = 0.f;
+            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int ff = 0; ff < 2 * kCW; ++ff) {
+                if (ml[ff].x == -INFINITY) continue;  // no entry, or no key: weight 0
+                const float w = ex2(ml[ff].x - M);
+                den = fmaf(w, ml[ff].y, den);
+                num.x = fmaf(w, v[ff].x, num.x);
+                num.y = fmaf(w, v[ff].y, num.y);
+                num.z = fmaf(w, v[ff].z, num.z);
+                num.w = fmaf(w, v[ff].w, num.w);
+            }
+            const int u = run.x, ub = u / a.Hv, ug = u % a.Hv;
+            if (run.z) {
+                const float inv = den > 0.f ? 1.f / den : 0.f;
+                if (h < unit_cols(a, ug) && PA_IN(row_off<D>(a, ub, ug, h) / D, a.out_rows, a.dev_status))
+                    *reinterpret_cast<float4*>(a.out + row_off<D>(a, ub, ug, h) + d4) =
+                        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+            } else if (PA_IN((long long)blockIdx.x + u, a.ws_slots, a.dev_status)) {
+                const long long slot = (long long)blockIdx.x + u;
+                *reinterpret_cast<float4*>(a.ws_acc + (slot * G + h) * D + d4) = num;
+                if (d4 == 0) *reinterpret_cast<float2*>(a.ws_ml + (slot * G + h) * 2) = make_float2(M, den);
+            }
+        }
+        if (a.finish) {
+            // Every CTA piece of this CTA is written (barrier); one thread per
+            // run orders them before counting them on the unit's counter
+            // (release), and the CTA whose count completes a unit merges the
+            // unit's CTA pieces, read through L2, in ascending CTA order (so
+            // the result does not depend on which CTA came last), then zeroes
+            // the counter.
+            __syncthreads();
+            if (threadIdx.x < nruns && !s_run[threadIdx.x].z) {
+                const int e = s_run[threadIdx.x].w;
+                const long long p0 = s_p0[e >> 1][e & 1];
+                long long c0 = ((p0 + 1) * n_cta - 1) / cost;  // CTA owning the unit's first page
+                const long long c1 = ((p0 + s_pb[e >> 1][e & 1]) * n_cta - 1) / cost;  // and its last
+                if (!PA_IN(c0, kMaxCounters, a.dev_status)) c0 = 0;
+                const unsigned seen = atom_add_acq_rel_gpu(a.ws_cnt + c0, 1u);
+                if (seen == unsigned(c1 - c0)) {
+                    s_fin[threadIdx.x] = make_int2(s_run[threadIdx.x].x, int(c0));
+                    s_fnp[threadIdx.x] = int(c1 - c0 + 1);
                 }
             }
             __syncthreads();
-            for (int idx = threadIdx.x; idx < G * D / 4; idx += kThreadsV1) {
-                const int h = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
-                float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-                uint32_t m = emask;
-                while (m) {  // two entries a step, in ascending order
-                    const int f0 = __ffs(m) - 1;
-                    m &= m - 1;
-                    const int f1 = m ? __ffs(m) - 1 : f0;
-                    const float w0 = s_w[h][f0], w1 = m ? s_w[h][f1] : 0.f;
-                    const float4 v0 = *reinterpret_cast<const float4*>(piece(f0) + h * kRow + d4);
-                    const float4 v1 = *reinterpret_cast<const float4*>(piece(f1) + h * kRow + d4);
-                    if (m) m &= m - 1;
-                    num.x = fmaf(w1, v1.x, fmaf(w0, v0.x, num.x));
-                    num.y = fmaf(w1, v1.y, fmaf(w0, v0.y, num.y));
-                    num.z = fmaf(w1, v1.z, fmaf(w0, v0.z, num.z));
-                    num.w = fmaf(w1, v1.w, fmaf(w0, v0.w, num.w));
-                }
-                const float M = s_md[h][0], den = s_md[h][1];
-                if (inside) {
-                    const float inv = den > 0.f ? 1.f / den : 0.f;
-                    if (h < unit_cols(a, ug))
-                        *reinterpret_cast<float4*>(a.out + row_off<D>(a, ub, ug, h) + d4) =
-                            make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-                } else {
-                    const long long slot = (long long)blockIdx.x + u;
-                    *reinterpret_cast<float4*>(a.ws_acc + (slot * G + h) * D + d4) = num;
-                    if (d4 == 0) *reinterpret_cast<float2*>(a.ws_ml + (slot * G + h) * 2) = make_float2(M, den);
-                }
+            for (int r = 0; r < nruns; ++r) {
+                const int u = s_fin[r].x;
+                if (u < 0) continue;
+                finish_unit<D>(a, u, s_fin[r].y, s_fnp[r]);
+                if (threadIdx.x == 0) a.ws_cnt[s_fin[r].y] = 0u;
             }
-            __syncthreads();  // s_w / s_md are reused by the next unit
+        }
+    }
+    if (kCtaMerge && a.finish) {
+        // Sequences with an invalid length have no work units: their rows are
+        // written as zeros here (the combine kernel does this otherwise).
+        for (long long b = blockIdx.x; b < a.B; b += n_cta) {
+            if (seq_pages(a, int(b), P) > 0) continue;
+            if (threadIdx.x == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
+            const int per_row = a.Hq * D / 4;
+            for (int i = threadIdx.x; i < a.Tl * per_row; i += kThreadsV1) {
+                const int t = i / per_row;
+                if (PA_IN((b * a.T + a.t0 + t) * a.Hq, a.out_rows, a.dev_status))
+                reinterpret_cast<float4*>(a.out + ((b * a.T + a.t0 + t) * a.Hq) * D)[i - t * per_row] =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
     }
 }
@@ -930,7 +1050,9 @@ __global__ void __launch_bounds__(D / DS * NG, 1024 / (D / DS * NG)) combine_v1(
         np = c1 > c0 ? int(c1 - c0 + 1) : 0;  // 0: finished inside one part
     }
     pdl_wait_primary();  // the partial kernel's pieces are complete from here on
-    float* o = a.out + (((long long)b * a.T + a.t0 + t) * a.Hq + hq) * D + d;
+    const long long orow = ((long long)b * a.T + a.t0 + t) * a.Hq + hq;
+    if (!PA_IN(orow, a.out_rows, a.dev_status)) return;
+    float* o = a.out + orow * D + d;
     if (pb == 0) {
         if (grp == 0) *o = 0.f;
         if (h == 0 && d == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
@@ -947,7 +1069,8 @@ __global__ void __launch_bounds__(D / DS * NG, 1024 / (D / DS * NG)) combine_v1(
         float mj = -INFINITY, lj = 0.f;
         if (lane < cnt) {
             const long long cc = c0 + x0 + lane;
-            if (T >= n || cc * T / n != (cc + 1) * T / n) {  // T >= n: no share is empty
+            if ((T >= n || cc * T / n != (cc + 1) * T / n) &&  // T >= n: no share is empty
+                PA_IN(cc + unit, a.ws_slots, a.dev_status)) {
                 const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((cc + unit) * a.G + r) * 2);
                 mj = ml.x;
                 lj = ml.y;
@@ -956,7 +1079,8 @@ __global__ void __launch_bounds__(D / DS * NG, 1024 / (D / DS * NG)) combine_v1(
         const float* accp = a.ws_acc + ((c0 + x0 + unit) * a.G + r) * D + d;
         float v[kBatch];
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j) v[j] = j < cnt ? accp[(long long)j * a.G * D] : 0.f;
+        for (int j = 0; j < kBatch; ++j)
+            v[j] = j < cnt && PA_IN(c0 + x0 + j + unit, a.ws_slots, a.dev_status) ? accp[(long long)j * a.G * D] : 0.f;
         const float Mn = fmaxf(M, warp_max(mj));
         if (Mn == -INFINITY) continue;  // no key so far
         const float sc = ex2(M - Mn);   // M = -inf -> 0
@@ -1066,7 +1190,7 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
         }
         if (e != cudaSuccess) return e;
     }
-    if (!(phases & 2)) return cudaSuccess;
+    if (!(phases & 2) || a.finish) return cudaSuccess;  // single launch: no combine kernel
     cudaLaunchConfig_t cfg = {};
     // Every combine CTA has 128 threads at most (8,192 registers), so one fits
     // beside a partial-kernel CTA and the next call's partial CTAs find room
@@ -1087,15 +1211,18 @@ cudaError_t launch_typed(const CUtensorMap& k, const CUtensorMap& v, const V1Par
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: (m, l) pairs, then accumulators, one slot per (part, unit) piece
-// of G columns; Hv units per sequence.
+// Workspace: the arrival counters of the single launch (a fixed block that
+// must be zero before a call and is left zero by it), then (m, l) pairs, then
+// accumulators, one slot per (part, unit) piece of G columns; Hv units per
+// sequence.
 struct WsLayout {
-    size_t ml, acc, total;
+    size_t cnt, ml, acc, total;
 };
 WsLayout ws_layout(int B, int Hv, int G, int D, int n_ctas) {
     const size_t slots = size_t(n_ctas) * kCW + size_t(B) * Hv;
     WsLayout w;
-    w.ml = 0;
+    w.cnt = 0;
+    w.ml = w.cnt + size_t(kMaxCounters) * sizeof(unsigned);
     w.acc = w.ml + round256(slots * G * 2 * sizeof(float));
     w.total = w.acc + slots * G * D * sizeof(float);
     return w;
@@ -1106,6 +1233,7 @@ WsLayout ws_layout(int B, int Hv, int G, int D, int n_ctas) {
 size_t decode_v1_workspace_bytes(int B, int Hkv, int G, int NB, int D, int n_ctas) {
     return ws_layout(B, Hkv * NB, G, D, n_ctas).total;
 }
+
 
 cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
@@ -1160,6 +1288,9 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     char* ws = static_cast<char*>(call.workspace);
     a.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
     a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
+    a.ws_cnt = reinterpret_cast<unsigned*>(ws + wl.cnt);
+    a.ws_slots = (long long)call.n_ctas * kCW + (long long)call.B * call.Hkv * NB;
+    a.q_rows = a.out_rows = (long long)call.B * T * call.Hq;
     a.dev_status = call.dev_status;
     a.B = call.B;
     a.Hq = call.Hq;
@@ -1179,6 +1310,7 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.n_ctas = call.n_ctas;
     a.window = call.window;
     a.cta_pieces = G <= 8 && D <= 128;  // as the partial kernel's kCtaMerge
+    a.finish = a.cta_pieces && call.phases == 3 && call.single_launch;  // one launch for the whole call
     a.k_new = call.k_new;
     a.v_new = call.v_new;
     a.k_cache = const_cast<void*>(call.k);
@@ -1191,7 +1323,7 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.unit_cost = kUnitCost;
     // at least one page tile per warp (head_dim 256 with 32-slot pages has
     // one: its K and V copies then take turns in it)
-    if (a.ntiles < kCW) return cudaErrorInvalidValue;
+    if (a.ntiles < kCW || call.n_ctas > kMaxCounters) return cudaErrorInvalidValue;
     const bool bf = call.dtype == PA_BF16;
 #define PA_V1_CASE(DD, PP)                                                                        \
     if (D == DD && P == PP)                                                                       \

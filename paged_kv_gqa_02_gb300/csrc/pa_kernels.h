@@ -10,9 +10,10 @@ namespace pa {
 cudaError_t launch_decode_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st);
 // v0 tile kernel over packed prefill rows; grid (ceil(max_q_len/4), Hkv, B).
 cudaError_t launch_prefill_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st);
-// Split combine, grid (Hq, B), D threads.
+// Split combine, grid (Hq, B), D threads; sequence b merges its first
+// splits_per_seq[b] splits (all S when NULL).
 cudaError_t launch_combine_v0(const float* ml, const float* acc, float* out, int B, int Hq,
-                              int S, int D, cudaStream_t st);
+                              int S, int D, cudaStream_t st, const int32_t* splits_per_seq = nullptr);
 
 // v1 decode for 16-bit K/V: persistent length-balanced partial kernel (TMA +
 // mma.sync) followed by a PDL-launched combine of split units.
@@ -36,6 +37,7 @@ struct DecodeV1Call {
     int row_block = 0;  // rows of a unit (0: row_count); row_block x Hq/Hkv <= 16.  The
                         // launch's rows come in blocks of row_block, each block a unit
     int window = 0;     // > 0: each row sees only its last `window` keys
+    int single_launch = 0;  // 1: finish split units in the partial kernel (one column tile, D <= 128)
     // KV append (both nullptr: none): [B][Hkv][D] rows written to row L_b - 1
     // of the cache and attended in place of what it held
     const void* k_new = nullptr;
@@ -55,7 +57,8 @@ cudaError_t launch_append_kv(const void* k_new, const void* v_new, void* k_cache
                              int64_t token_stride, int64_t head_stride, cudaStream_t st);
 
 // Hq counts q heads times query rows per sequence.
-// Workspace of a launch whose units have G columns, NB row blocks per kv head.
+// Workspace of a launch whose units have G columns, NB row blocks per kv head;
+// its first PA_DECODE_COUNTER_BYTES hold the single launch's arrival counters.
 size_t decode_v1_workspace_bytes(int B, int Hkv, int G, int NB, int D, int n_ctas);
 cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st);
 

@@ -72,5 +72,5 @@ PA_EXPORT pa_status pa_decode_noalloc(const pa_params* p, const void* q, const v
     st = pa_decode_partial(p, q, k_cache, v_cache, block_tables, context_lens, ml, acc, S,
                            dev_status, stream);
     if (st != PA_OK) return st;
-    return pa_combine(p, ml, acc, S, out, stream);
+    return pa_combine(p, ml, acc, S, nullptr, out, stream);
 }

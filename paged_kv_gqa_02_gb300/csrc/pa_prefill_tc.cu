@@ -82,6 +82,7 @@ struct TcParams {
     uint32_t* dev_status;
     int32_t Hq, Hkv, G, tq, P, num_pages, max_blocks, max_q_len, total_q;
     int32_t n_pairs;  // row-tile pairs per (sequence, kv head)
+    int32_t B;        // sequences
     int32_t head_first;
     float scale_log2;  // > 0
 };
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = a.G, P = a.P, tq = a.tq;
 
     // ---- rows of the two tiles and their causal ends ----------------------------
+    if (!PA_IN(b, a.B, a.dev_status)) return;  // the whole CTA, before any barrier
     const int L = a.context_lens[b];
     const int row0 = a.cu_q_lens[b];
     const int Tq = a.cu_q_lens[b + 1] - row0;
@@ -184,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = i / (G * (kD / 4)), rest = i % (G * (kD / 4));
             const int h = rest / (kD / 4), c = rest % (kD / 4);
             float* o = a.out + (int64_t(row0 + r_first + r) * a.Hq + g * G + h) * kD;
-            reinterpret_cast<float4*>(o)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (PA_IN(row0 + r_first + r, a.total_q, a.dev_status))
+                reinterpret_cast<float4*>(o)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         return;
     }
@@ -274,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // physical page of lane's slot in tile j (out-of-pool entries flagged, read as zeros)
             int pg = a.num_pages;  // beyond the tensor: the box reads as zeros
             const int idx = j * PT + lane;
-            if (lane < PT && idx < npg) {
+            if (lane < PT && idx < npg && PA_IN(idx, a.max_blocks, a.dev_status)) {
                 const int e = table[idx];
                 if (e >= 0 && e < a.num_pages)
                     pg = e;
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool pok = true;
             {
                 const int idx = j * PT + lane;
-                if (lane < PT && idx < npg) {
+                if (lane < PT && idx < npg && PA_IN(idx, a.max_blocks, a.dev_status)) {
                     const int e = __ldg(table + idx);
                     pok = e >= 0 && e < a.num_pages;
                 }
@@ -520,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::ld_32x32b_x32(obase + 32 * c, ra);
                 tc::wait_ld();
                 tc::reg_fence(ra);
-                if (row_ok) {
+                if (row_ok && PA_IN(row0 + r_tile + t, a.total_q, a.dev_status)) {
                     float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
@@ -641,6 +644,7 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cuda
     p.max_blocks = a.max_blocks_per_seq;
     p.max_q_len = a.max_q_len;
     p.total_q = a.total_q;
+    p.B = a.num_seqs;
     p.head_first = head_first;
     p.scale_log2 = a.scale_log2;
     const int64_t n_pairs = (a.max_q_len + 2 * tq - 1) / (2 * tq);  // pairs of row tiles

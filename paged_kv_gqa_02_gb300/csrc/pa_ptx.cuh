@@ -203,6 +203,16 @@ __device__ inline void mma_1688(float* c, uint32_t a0, uint32_t a1, uint32_t b0)
     }
 }
 
+// ---- inter-CTA counters ------------------------------------------------------------
+// atomicAdd with release and acquire semantics at GPU scope: the CTA's writes
+// ordered before it (by a CTA barrier) are visible to whoever reads the count
+// it leaves, and the writes of the arrivals it reads are visible after it.
+__device__ inline unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // ---- programmatic dependent launch -------------------------------------------------
 __device__ inline void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

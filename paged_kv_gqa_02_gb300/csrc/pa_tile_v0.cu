@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
     pdl_wait_primary();  // the previous kernel's writes are visible from here on
 
     // ---- rows of this tile and their causal ends --------------------------
-    int L = a.context_lens[b];
+    int L = PA_IN(b, a.num_seqs, a.dev_status) ? a.context_lens[b] : 0;
     int row0, Tq;  // first packed row, rows of this sequence
     if (decode) {
         row0 = b;
@@ -72,8 +72,9 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
         row0 = b * a.rows_per_seq;
         Tq = a.rows_per_seq;
     } else {
-        row0 = a.cu_q_lens[b];
-        Tq = a.cu_q_lens[b + 1] - row0;
+        const bool in = PA_IN(b + 1, a.num_seqs + 1, a.dev_status);
+        row0 = in ? a.cu_q_lens[b] : 0;
+        Tq = in ? a.cu_q_lens[b + 1] - row0 : 0;
     }
     const bool bad = (Tq < 0) || (row0 < 0) || (L < Tq) || (L > a.max_blocks_per_seq * P) ||
                      (!decode && Tq > a.max_q_len);
@@ -122,7 +123,9 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
         }
     };
     // The first table entry does not wait for the length: its index is known.
-    const int32_t first = t0 / P < a.max_blocks_per_seq ? table[t0 / P] : -1;
+    const int32_t first = t0 / P < a.max_blocks_per_seq && PA_IN(t0 / P, a.max_blocks_per_seq, a.dev_status)
+                              ? table[t0 / P]
+                              : -1;
     int32_t next = t0 < t1 ? first : -1;
     if (t0 < t1 && valid(next)) fetch(next, t0);  // in flight while q is staged
 
@@ -132,7 +135,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
         float x = 0.f;
         if (r < n_rows) {
             const int64_t qi = (int64_t(row0 + r_first + r) * Hq + g * G + h) * D + d;
-            x = Elt<T>::f(static_cast<const T*>(a.q)[qi]) * a.scale_log2;
+            if (PA_IN(qi, a.q_elems, a.dev_status)) x = Elt<T>::f(static_cast<const T*>(a.q)[qi]) * a.scale_log2;
         }
         q_s[dist * D + d] = x;
     }
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
                 }
             }
         }
-        next = ps + P < t1 ? table[(ps + P) / P] : -1;
+        next = ps + P < t1 && PA_IN((ps + P) / P, a.max_blocks_per_seq, a.dev_status) ? table[(ps + P) / P] : -1;
         if (!valid(page)) {
             if (tid == 0) flag(a.dev_status, PA_DEV_BAD_PAGE);
             if (ps + P < t1 && valid(next)) fetch(next, ps + P);
@@ -232,6 +235,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
                 const int r = dist / G, h = dist % G;
                 if (r < n_rows) {
                     const int64_t idx = (int64_t(row0 + r_first + r) * Hq + g * G + h) * Sn + split;
+                    if (!PA_IN(idx, a.partial_items, a.dev_status)) continue;
                     if (m_s[dist] != -INFINITY) a.partial_acc[idx * D + my_d] = acc[k];
                     if (my_d == 0) {
                         a.partial_ml[idx * 2] = m_s[dist];
@@ -249,16 +253,19 @@ __global__ void __launch_bounds__(kThreads) attn_tile_v0(AttnArgs a) {
                 if (r < n_rows) {
                     const float l = l_s[dist];
                     const int64_t oi = (int64_t(row0 + r_first + r) * Hq + g * G + h) * D + my_d;
-                    a.out[oi] = l > 0.f ? acc[k] / l : 0.f;
+                    if (PA_IN(oi, a.out_elems, a.dev_status)) a.out[oi] = l > 0.f ? acc[k] / l : 0.f;
                 }
             }
         }
     }
 }
 
-// Combine: one CTA per (q head, sequence), one thread per output dim.
+// Combine: one CTA per (q head, sequence), one thread per output dim.  The
+// partials are [B][Hq][S][...]; sequence b merges its first S_b splits, S_b =
+// splits_per_seq[b] clamped to [0, S] (all S when splits_per_seq is NULL).
 __global__ void combine_v0(const float* __restrict__ ml, const float* __restrict__ acc,
-                           float* __restrict__ out, int Hq, int S, int D) {
+                           float* __restrict__ out, int Hq, int S, int D,
+                           const int32_t* __restrict__ splits_per_seq) {
     // Batches of 32 splits: lane j holds split x0 + j's (m, l), every thread
     // loads its dim of all 32 accumulators at once; batches are merged by
     // rescaling in ascending split order (fixed shuffle trees, no atomics).
@@ -267,9 +274,10 @@ __global__ void combine_v0(const float* __restrict__ ml, const float* __restrict
     pdl_wait_primary();  // the partials are complete from here on
     const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31;
     const int64_t base = (int64_t(b) * Hq + h) * S;
+    const int Sb = splits_per_seq ? min(max(splits_per_seq[b], 0), S) : S;  // splits of this sequence
     float M = -INFINITY, num = 0.f, den = 0.f;
-    for (int x0 = 0; x0 < S; x0 += kB) {
-        const int cnt = min(kB, S - x0);
+    for (int x0 = 0; x0 < Sb; x0 += kB) {
+        const int cnt = min(kB, Sb - x0);
         float mj = -INFINITY, lj = 0.f;
         if (lane < cnt) {
             const float2 v = *reinterpret_cast<const float2*>(ml + (base + x0 + lane) * 2);
@@ -341,12 +349,25 @@ cudaError_t dispatch_t(const AttnArgs& a, pa_dtype dt, int D, int P, dim3 grid, 
 
 }  // namespace
 
-cudaError_t launch_decode_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st) {
+namespace {
+// The buffers' extents (total_q rows of Hq x D; split partials per row and
+// q head), for the checked build's range checks.
+AttnArgs with_extents(const AttnArgs& in, int D) {
+    AttnArgs a = in;
+    a.q_elems = a.out_elems = int64_t(a.total_q) * a.num_q_heads * D;
+    a.partial_items = int64_t(a.total_q) * a.num_q_heads * (a.num_splits > 0 ? a.num_splits : 1);
+    return a;
+}
+}  // namespace
+
+cudaError_t launch_decode_v0(const AttnArgs& in, pa_dtype dt, int D, int P, cudaStream_t st) {
+    const AttnArgs a = with_extents(in, D);
     dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
     return dispatch_t<1>(a, dt, D, P, grid, st);
 }
 
-cudaError_t launch_prefill_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st) {
+cudaError_t launch_prefill_v0(const AttnArgs& in, pa_dtype dt, int D, int P, cudaStream_t st) {
+    const AttnArgs a = with_extents(in, D);
     constexpr int R = 4;
     const int splits = a.out == nullptr ? a.num_splits : 1;  // split partials: multi-row decode only
     if (splits < 1 || (splits > 1 && a.cu_q_lens != nullptr)) return cudaErrorInvalidValue;
@@ -355,7 +376,7 @@ cudaError_t launch_prefill_v0(const AttnArgs& a, pa_dtype dt, int D, int P, cuda
 }
 
 cudaError_t launch_combine_v0(const float* ml, const float* acc, float* out, int B, int Hq,
-                              int S, int D, cudaStream_t st) {
+                              int S, int D, cudaStream_t st, const int32_t* splits_per_seq) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(Hq, B);
     cfg.blockDim = dim3(D);
@@ -365,7 +386,7 @@ cudaError_t launch_combine_v0(const float* ml, const float* acc, float* out, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_v0, ml, acc, out, Hq, S, D);
+    return cudaLaunchKernelEx(&cfg, combine_v0, ml, acc, out, Hq, S, D, splits_per_seq);
 }
 
 namespace {

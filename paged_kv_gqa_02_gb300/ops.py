@@ -12,17 +12,19 @@ import os
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libpaged_gqa.so")
+# PA_GQA_LIB names another build of the library (e.g. the checked build)
+LIB_PATH = os.environ.get("PA_GQA_LIB") or os.path.join(PKG, "libpaged_gqa.so")
 
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 DTYPE_CODE = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16}
-PA_DEV_BAD_PAGE, PA_DEV_BAD_LEN, PA_DEV_TIMEOUT = 1, 2, 4
+PA_DEV_BAD_PAGE, PA_DEV_BAD_LEN, PA_DEV_TIMEOUT, PA_DEV_OOB = 1, 2, 4, 8
 STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_DTYPE",
           4: "PA_ERR_ALIGN", 5: "PA_ERR_WORKSPACE", 6: "PA_ERR_UNSUPPORTED", 7: "PA_ERR_CUDA"}
 
 EXPORTS = ("pa_params_init", "pa_status_string", "pa_decode_plan", "pa_decode_workspace_size",
            "pa_decode", "pa_decode_partial", "pa_combine", "pa_prefill_workspace_size",
-           "pa_prefill_chunk", "pa_version")
+           "pa_prefill_chunk", "pa_version", "pa_decode_append", "pa_decode_noalloc",
+           "pa_build_flags")
 
 
 class PaError(RuntimeError):
@@ -42,7 +44,8 @@ class Params(ctypes.Structure):
                 ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("deterministic", ctypes.c_int32),
                 ("num_splits", ctypes.c_int32), ("decode_phases", ctypes.c_int32),
-                ("decode_q_rows", ctypes.c_int32), ("sliding_window", ctypes.c_int32)]
+                ("decode_q_rows", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
+                ("single_launch", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -69,7 +72,7 @@ def load(path: str = LIB_PATH):
             L.pa_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             L.pa_decode_partial.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
             L.pa_decode_append.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
-            L.pa_combine.argtypes = [P, vp, vp, i32, vp, vp]
+            L.pa_combine.argtypes = [P, vp, vp, i32, vp, vp, vp]
             L.pa_prefill_workspace_size.argtypes = [P, i32, i32]
             L.pa_prefill_workspace_size.restype = sz
             L.pa_prefill_chunk.argtypes = [P, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
@@ -78,6 +81,7 @@ def load(path: str = LIB_PATH):
                          "pa_combine", "pa_prefill_chunk", "pa_decode_noalloc"):
                 getattr(L, name).restype = ctypes.c_int
             L.pa_version.restype = i32
+            L.pa_build_flags.restype = i32
             _lib = L
     return _lib
 
@@ -85,7 +89,7 @@ def load(path: str = LIB_PATH):
 def make_params(*, num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                 max_blocks_per_seq, max_context_len, scale=None, dtype="bf16", kv_dtype=None,
                 deterministic=1, num_splits=0, strides=(0, 0, 0), decode_phases=0,
-                decode_q_rows=0, sliding_window=0) -> Params:
+                decode_q_rows=0, sliding_window=0, single_launch=0) -> Params:
     p = Params()
     load().pa_params_init(ctypes.byref(p))
     p.num_seqs, p.num_q_heads, p.num_kv_heads = num_seqs, num_q_heads, num_kv_heads
@@ -100,6 +104,7 @@ def make_params(*, num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num
     p.decode_phases = decode_phases
     p.decode_q_rows = decode_q_rows
     p.sliding_window = sliding_window
+    p.single_launch = single_launch
     return p
 
 
@@ -158,7 +163,7 @@ def decode(p: Params, q, k_cache, v_cache, block_tables, context_lens, out=None,
         out = _empty_out(q, p)
     if workspace is None:
         n = decode_workspace_size(p)
-        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device) if n else None
+        workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=q.device) if n else None
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().pa_decode(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                             _ptr(block_tables), _ptr(context_lens), _ptr(out), _ptr(workspace),
@@ -175,7 +180,7 @@ def decode_append(p: Params, q, k_new, v_new, k_cache, v_cache, block_tables, co
         out = _empty_out(q, p)
     if workspace is None:
         n = decode_workspace_size(p)
-        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device) if n else None
+        workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=q.device) if n else None
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().pa_decode_append(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                    _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), _ptr(out),
@@ -192,9 +197,11 @@ def decode_partial(p: Params, q, k_cache, v_cache, block_tables, context_lens, p
                                     _stream(stream)), "pa_decode_partial")
 
 
-def combine(p: Params, partial_ml, partial_acc, num_splits, out, stream=None):
+def combine(p: Params, partial_ml, partial_acc, num_splits, out, stream=None, splits_per_seq=None):
+    """pa_combine: num_splits is the partials' split stride (max_splits);
+    splits_per_seq (device int32 [B], optional) limits each sequence."""
     _check(load().pa_combine(ctypes.byref(p), _ptr(partial_ml), _ptr(partial_acc), num_splits,
-                             _ptr(out), _stream(stream)), "pa_combine")
+                             _ptr(splits_per_seq), _ptr(out), _stream(stream)), "pa_combine")
     return out
 
 

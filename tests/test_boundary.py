@@ -43,6 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in declared_functions():
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
     assert lib.pa_version() >= 100
+    assert lib.pa_build_flags() == 0  # the release build: no range checks compiled in
 
 
 def test_params_struct_layout_matches_header(lib):
@@ -107,7 +108,8 @@ def call_decode(p, q=FAKE, out=FAKE, bt=FAKE, ws=None, nbytes=0):
     ("max_context_len", 16 * 32 + 1, 2), ("num_pages", 0, 2), ("q_dtype", 9, 3),
     ("kv_dtype", ops.PA_F16, 6), ("out_dtype", ops.PA_BF16, 6), ("deterministic", 2, 2),
     ("num_splits", -1, 2), ("head_stride", 4, 4), ("token_stride", 100, 4),
-    ("decode_phases", 4, 2), ("decode_phases", -1, 2),
+    ("decode_phases", 4, 2), ("decode_phases", -1, 2), ("single_launch", 2, 2),
+    ("single_launch", -1, 2),
 ])
 def test_rejects_bad_params(lib, field, value, code):
     p = base_params()
@@ -122,6 +124,25 @@ def test_rejects_null_and_misaligned(lib):
     assert call_decode(p, q=None) == 1
     assert call_decode(p, out=ctypes.c_void_p((1 << 20) + 4)) == 4
     assert call_decode(p, bt=ctypes.c_void_p((1 << 20) + 2)) == 4
+
+
+def test_combine_host_checks(lib):
+    """pa_combine rejects NULL pointers, a split stride below 1, head_dim 256
+    and misaligned partials, out or split counts before launching."""
+    p = base_params()
+    L = ops.load()
+    big = ctypes.c_void_p(1 << 20)
+
+    def call(ml=big, acc=big, S=4, spl=None, out=big):
+        return L.pa_combine(ctypes.byref(p), ml, acc, S, spl, out, None)
+    assert call(ml=None) == 1 and call(acc=None) == 1 and call(out=None) == 1
+    assert call(S=0) == 2
+    assert call(acc=ctypes.c_void_p((1 << 20) + 8)) == 4
+    assert call(out=ctypes.c_void_p((1 << 20) + 4)) == 4
+    assert call(ml=ctypes.c_void_p((1 << 20) + 4)) == 4
+    assert call(spl=ctypes.c_void_p((1 << 20) + 2)) == 4
+    p.head_dim = 256
+    assert call() == 6
 
 
 def test_rejects_small_workspace(lib):
