@@ -146,6 +146,16 @@ typedef struct {
                                    merges the pieces (see pa_decode).  0 (the
                                    default) = partial kernel + combine kernel,
                                    the faster form on GB300.                     */
+    int32_t debug_timeout;      /* testing only, 0 otherwise.  1: every wait of
+                                   the split-KV decode kernel and of the tensor-
+                                   core prefill kernel gives up at once, before
+                                   any copy is issued (each first waits with no
+                                   time allowed on a barrier that no copy
+                                   targets), so the kernels take their
+                                   timeout path: PA_DEV_TIMEOUT is set, nothing
+                                   is read from the cache and the results are
+                                   void (zeros).  Shows that a wait that runs
+                                   out leaves the context usable.               */
 } pa_params;
 
 /* Fills *p with defaults: contiguous strides, PA_F32 out, automatic splits,

@@ -52,6 +52,7 @@ pa_status check_params(const pa_params* p, Resolved* r) {
     if (p->decode_q_rows > p->max_context_len) return PA_ERR_SHAPE;
     if (p->sliding_window < 0) return PA_ERR_SHAPE;
     if (p->single_launch != 0 && p->single_launch != 1) return PA_ERR_SHAPE;
+    if (p->debug_timeout != 0 && p->debug_timeout != 1) return PA_ERR_SHAPE;
     const int64_t D = p->head_dim;
     r->head_stride = p->head_stride ? p->head_stride : D;
     r->token_stride = p->token_stride ? p->token_stride : p->num_kv_heads * r->head_stride;
@@ -331,6 +332,8 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         c.row_count = rows;
         c.row_block = rb;  // blocks of rows are units of one launch
         c.single_launch = p->single_launch;
+        c.max_context_len = p->max_context_len;
+        c.debug_timeout = p->debug_timeout;
         return cuda_status(pa::launch_decode_v1(c, stream));
     }
     if (p->sliding_window > 0) return PA_ERR_UNSUPPORTED;  // windows: split-KV kernel only
@@ -447,6 +450,7 @@ PA_EXPORT pa_status pa_prefill_chunk(const pa_params* p, const void* q, const in
     a.max_q_len = max_q_len;
     a.total_q = total_q;
     a.num_splits = 1;
+    a.debug_timeout = p->debug_timeout;
     if (pa::prefill_tc_supported(p->kv_dtype, p->head_dim, p->page_size, r.group, p->scale))
         return cuda_status(pa::launch_prefill_tc(a, p->kv_dtype, p->head_dim, p->page_size, stream));
     return cuda_status(pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));

@@ -37,6 +37,7 @@ struct AttnArgs {
     int32_t rows_per_seq = 0;  // > 1 with cu_q_lens == nullptr: sequence b owns rows b*n .. b*n + n - 1
     // Extents, in elements, for the checked build's range checks
     int64_t q_elems = 0, out_elems = 0, partial_items = 0;
+    int32_t debug_timeout = 0;  // 1: the tensor-core prefill gives up before any copy (testing)
 };
 
 // ---- element conversions -------------------------------------------------

@@ -57,6 +57,7 @@ constexpr int kCtaMergeMaxShare = 16;         // CTA merge only while CTA shares
 // c0 (each CTA boundary is crossed by at most one unit), so the counters take
 // a fixed block at the start of the workspace whatever the call's sizes.
 constexpr int kMaxCounters = int(PA_DECODE_COUNTER_BYTES / sizeof(unsigned));
+constexpr int kDeadPage = -2;  // static plan: a page past the sequence's length (skipped, not an error)
 
 struct V1Params {
     const void* q;  // [B*Hq][D]
@@ -71,6 +72,12 @@ struct V1Params {
     uint32_t* dev_status;
     int32_t B, Hq, Hkv, G, num_pages, max_blocks, max_len;
     int32_t window;     // > 0: a row sees only its last `window` keys
+    // > 0 (small calls): the partition counts every sequence at this many
+    // pages, so it follows from host parameters alone and a warp loads its
+    // lengths and table entries in one round trip; pages past a sequence's
+    // length are skipped (their ring slots are armed with no bytes)
+    int32_t static_pages;
+    int32_t debug_timeout;  // 1: each warp's first wait (on a barrier no copy targets) gives up at once
     int32_t T, t0, Gq;  // query rows per sequence, first row of this launch, q heads per kv head
     // Row blocks: the launch's Tl rows come in NB blocks of rb rows (the last
     // may be shorter), each block its own unit.  Unit (b, u), u < Hv = Hkv * NB,
@@ -129,6 +136,10 @@ __device__ inline int first_page(const V1Params& a, int L, int P) {
     return lo > 0 ? lo / P : 0;
 }
 
+// Pages of sequence b in the work partition: its own (seq_pages) or, with
+// a static plan, the same count for every sequence.
+__device__ inline int part_pages(const V1Params& a, int b, int P);
+
 // Kv head, first row and columns of unit u (a row block of a kv head).
 __device__ inline int unit_head(const V1Params& a, int u) { return a.NB == 1 ? u : u / a.NB; }
 __device__ inline int unit_row0(const V1Params& a, int u) { return a.NB == 1 ? a.t0 : a.t0 + (u % a.NB) * a.rb; }
@@ -142,6 +153,10 @@ __device__ inline int seq_pages(const V1Params& a, int b, int P) {
     const int L = PA_IN(b, a.B, a.dev_status) ? __ldg(a.context_lens + b) : 0;
     const int n = pages_of_len(L, P, a.max_len, a.T);
     return n > 0 ? n - first_page(a, L, P) : 0;
+}
+
+__device__ inline int part_pages(const V1Params& a, int b, int P) {
+    return a.static_pages > 0 ? a.static_pages : seq_pages(a, b, P);
 }
 
 // Offset (elements) of column c of unit (b, u) in q and out: [B][T][Hq][D].
@@ -184,7 +199,7 @@ __device__ inline long long warp_incl_scan_ll(long long v, int lane) {
 __device__ inline long long total_cost(const V1Params& a, int P) {
     long long tot = 0;
     for (int b = threadIdx.x & 31; b < a.B; b += 32) {
-        const int pb = seq_pages(a, b, P);
+        const int pb = part_pages(a, b, P);
         if (pb > 0) tot += (long long)a.Hv * (pb + a.unit_cost);
     }
     return warp_sum_ll(tot);
@@ -198,7 +213,7 @@ __device__ inline Walk walk_start(const V1Params& a, int P, long long s, long lo
     long long basep = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int b = b0 + lane;
-        const int pb = b < a.B ? seq_pages(a, b, P) : 0;
+        const int pb = b < a.B ? part_pages(a, b, P) : 0;
         const long long c = pb > 0 ? (long long)a.Hv * (pb + W) : 0;
         const long long incl = warp_incl_scan_ll(c, lane);
         const long long total = __shfl_sync(0xffffffffu, incl, 31);
@@ -231,7 +246,7 @@ __device__ inline void walk_next_unit(Walk& w, const V1Params& a, int P) {
         int pb = 0;
         do {
             ++w.b;
-        } while (w.b < a.B && (pb = seq_pages(a, w.b, P)) == 0);
+        } while (w.b < a.B && (pb = part_pages(a, w.b, P)) == 0);
         if (w.b >= a.B) {
             w.done = 1;
             return;
@@ -370,6 +385,18 @@ __device__ inline void window_fill(LoadWindow& lw, const V1Params& a, int P) {
     walk_advance(x, i, threadIdx.x & 31, a, P);
     lw.live = x.done ? 0 : 1;
     lw.g = x.g;
+    if (a.static_pages > 0) {
+        // Static plan: the length and the table entry load together (entries
+        // up to max_blocks lie in the caller's table row; one past the
+        // sequence's pages is never used, and its page never read).
+        const bool in = lw.live && PA_IN(i, a.max_blocks, a.dev_status);
+        const int e = in ? __ldg(a.block_tables + (long long)x.b * a.max_blocks + i) : -1;
+        const int L = lw.live ? __ldg(a.context_lens + x.b) : 0;
+        const int n = pages_of_len(L, P, a.max_len, a.T);
+        if (lw.live && n == 0 && i == 0 && x.g == 0) flag(a.dev_status, PA_DEV_BAD_LEN);
+        lw.page = !in ? -1 : (i < n ? e : kDeadPage);
+        return;
+    }
     const int fpg = lw.live ? first_page(a, __ldg(a.context_lens + x.b), P) : 0;
     lw.page = lw.live && PA_IN(fpg + i, a.max_blocks, a.dev_status)
                   ? __ldg(a.block_tables + (long long)x.b * a.max_blocks + fpg + i)
@@ -396,8 +423,6 @@ __global__ void __maxnreg__(224)
                                                ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    pdl_launch_dependents();
-
     // ---- set-up that touches no global memory: it may overlap the kernel
     // before this one (programmatic dependent launch) ----------------------------
     int* tile_page = reinterpret_cast<int*>(base + size_t(a.ntiles) * kTile);  // [kMaxTiles]
@@ -408,6 +433,7 @@ __global__ void __maxnreg__(224)
     __shared__ int s_pb[kCW][2];        // and its page count
     __shared__ int4 s_run[2 * kCW];     // CTA merge: (unit, entry mask, inside, first entry) of each run
     __shared__ int s_nruns;
+    __shared__ __align__(8) uint64_t s_never;  // a barrier no copy or thread ever arrives on (debug_timeout)
     __shared__ int2 s_fin[2 * kCW];     // single launch: (unit, first CTA) of each run this CTA completes
     __shared__ int s_fnp[2 * kCW];      // and its CTA pieces
     if (threadIdx.x < 2 * kCW) s_fin[threadIdx.x] = make_int2(-1, 0);
@@ -418,6 +444,7 @@ __global__ void __maxnreg__(224)
         } else {  // rings are cut once the call's size is known: every tile's barrier
             for (int s = warp; s < a.ntiles; s += kCW) mbar_init(&tile_full[s], 1);
         }
+        if (warp == 0) mbar_init(&s_never, 1);
         mbar_fence_init();
         if (warp == 0) {
             tma_prefetch_desc(&tmK);
@@ -427,6 +454,9 @@ __global__ void __maxnreg__(224)
     }
     __syncwarp();
     pdl_wait_primary();  // the previous kernel's writes are visible from here on
+    // Only now may the combine kernel start: it reads the lengths before its
+    // own wait, and they are complete once the kernel before this one is.
+    pdl_launch_dependents();
 
     // ---- this CTA's share of the cost space, and this warp's part of it ---------
     const long long cost = total_cost(a, P);
@@ -462,6 +492,15 @@ __global__ void __maxnreg__(224)
     // issued and [x_stop, n_issued) may still be in flight.
     bool timed_out = false;
     int n_issued = 0, x_stop = 0;
+    if (a.debug_timeout) {
+        // Testing: a wait that runs out before any copy is issued (on a barrier
+        // nothing targets, with no time allowed) takes the timeout path below.
+        __syncthreads();  // s_never is initialised
+        if (!__all_sync(0xffffffffu, mbar_wait_ns(&s_never, 0, 0))) {
+            timed_out = true;
+            if (lane == 0) flag(a.dev_status, PA_DEV_TIMEOUT);
+        }
+    }
     auto issue = [&](int hx) {
         const int j = hx >> 1;
         while (j >= lw.base + 32) {  // next 32 pages of the share
@@ -478,7 +517,7 @@ __global__ void __maxnreg__(224)
         if (lane == 0) {
             const int slot = hx % NH;
             const bool ok = pg >= 0 && pg < a.num_pages;
-            if (!ok && (hx & 1) == 0) flag(a.dev_status, PA_DEV_BAD_PAGE);
+            if (!ok && pg != kDeadPage && (hx & 1) == 0) flag(a.dev_status, PA_DEV_BAD_PAGE);
             my_page[slot] = ok ? pg : -1;
             mbar_arrive_expect_tx(&my_full[slot], ok ? kTile : 0);
             if (ok) {
@@ -493,7 +532,7 @@ __global__ void __maxnreg__(224)
         }
         __syncwarp();
     };
-    if (!wk.done)
+    if (!wk.done && !timed_out)
         for (int hx = 0; hx < NH; ++hx) issue(hx);  // fill the ring
 
     // ---- compute side: S^T = K Q^T and O^T += V^T P^T ---------------------------
@@ -1030,23 +1069,24 @@ __global__ void __launch_bounds__(D / DS * NG, 1024 / (D / DS * NG)) combine_v1(
     const int W = a.unit_cost;
     long long T = 0, pre = 0;
     for (int x = lane; x < a.B; x += 32) {
-        const int pg = seq_pages(a, x, P);
+        const int pg = part_pages(a, x, P);
         const long long c = pg > 0 ? (long long)a.Hv * (pg + W) : 0;
         T += c;
         if (x < b) pre += c;
     }
     T = warp_sum_ll(T);
     pre = warp_sum_ll(pre);
-    const int pb = seq_pages(a, b, P);
+    const int pp = part_pages(a, b, P);  // the unit's pages in the partition
+    const int pb = seq_pages(a, b, P);   // 0: an invalid length
     const long long nc = ctas_in_use(T > 0 ? T : 1, a.n_ctas);
     const bool cta = a.cta_pieces && T <= (long long)kCtaMergeMaxShare * nc;  // as the partial kernel
     const long long n = cta ? nc : nc * warps_in_use(T, nc);  // parts of the piece partition
     long long c0 = 0;
     int np = 0;
-    if (pb > 0) {  // the unit's pages sit at cost positions [p0, p0 + pb)
-        const long long p0 = pre + (long long)g * (pb + W) + W;
+    if (pb > 0) {  // the unit's pages sit at cost positions [p0, p0 + pp)
+        const long long p0 = pre + (long long)g * (pp + W) + W;
         c0 = ((p0 + 1) * n - 1) / T;  // part v owns [v*T/n, (v+1)*T/n)
-        const long long c1 = ((p0 + pb) * n - 1) / T;
+        const long long c1 = ((p0 + pp) * n - 1) / T;
         np = c1 > c0 ? int(c1 - c0 + 1) : 0;  // 0: finished inside one part
     }
     pdl_wait_primary();  // the partial kernel's pieces are complete from here on
@@ -1309,6 +1349,16 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     a.scale_log2 = call.scale_log2;
     a.n_ctas = call.n_ctas;
     a.window = call.window;
+    a.debug_timeout = call.debug_timeout;
+    // Static plan for small calls (no window, no append): every sequence
+    // counts max_context_len's pages in the partition when that whole space
+    // is a small call (shares of at most kCtaMergeMaxShare cost units).
+    {
+        const long long pmax = (call.max_context_len + P - 1) / P;
+        const bool small = (long long)call.B * a.Hv * (pmax + kUnitCost) <=
+                           (long long)kCtaMergeMaxShare * call.n_ctas;
+        a.static_pages = call.window == 0 && call.k_new == nullptr && small && pmax > 0 ? int(pmax) : 0;
+    }
     a.cta_pieces = G <= 8 && D <= 128;  // as the partial kernel's kCtaMerge
     a.finish = a.cta_pieces && call.phases == 3 && call.single_launch;  // one launch for the whole call
     a.k_new = call.k_new;

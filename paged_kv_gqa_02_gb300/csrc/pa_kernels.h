@@ -38,6 +38,8 @@ struct DecodeV1Call {
                         // launch's rows come in blocks of row_block, each block a unit
     int window = 0;     // > 0: each row sees only its last `window` keys
     int single_launch = 0;  // 1: finish split units in the partial kernel (one column tile, D <= 128)
+    int max_context_len = 0;  // host bound on every length (sizes the static plan of small calls)
+    int debug_timeout = 0;    // 1: every warp's waits give up before any copy is issued (testing)
     // KV append (both nullptr: none): [B][Hkv][D] rows written to row L_b - 1
     // of the cache and attended in place of what it held
     const void* k_new = nullptr;

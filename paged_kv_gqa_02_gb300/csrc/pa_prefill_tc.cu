@@ -63,7 +63,7 @@ constexpr uint32_t kQOff = 0;                  // Q of A, then Q of B
 constexpr uint32_t kKOff = kQOff + 2 * kTileBytes;
 constexpr uint32_t kVOff = kKOff + kKS * kTileBytes;
 constexpr uint32_t kBarOff = kVOff + kVS * kTileBytes;
-constexpr uint32_t kNumBars = 1 + 2 * kKS + 2 * kVS + 2 * 3 + 1;
+constexpr uint32_t kNumBars = 1 + 2 * kKS + 2 * kVS + 2 * 3 + 2;
 constexpr uint32_t kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
 constexpr uint64_t kWaitNs = 2000000000ull;     // a role gives up after 2 s on one barrier
 constexpr uint32_t kSleepNs = 20000;            // longest sleep inside one try_wait
@@ -83,6 +83,7 @@ struct TcParams {
     int32_t Hq, Hkv, G, tq, P, num_pages, max_blocks, max_q_len, total_q;
     int32_t n_pairs;  // row-tile pairs per (sequence, kv head)
     int32_t B;        // sequences
+    int32_t debug_timeout;  // 1: the CTA's first wait (on a barrier no copy targets) gives up at once
     int32_t head_first;
     float scale_log2;  // > 0
 };
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&o_done[i], 1);
         }
         mbar_init(mma_done, 1);
+        mbar_init(mma_done + 1, 1);  // never arrived on: the debug_timeout wait
         *abort_flag = 0u;
         mbar_fence_init();
     }
@@ -246,11 +248,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = *tslot;
+    if (a.debug_timeout) {
+        // Testing: a wait that runs out before any copy is issued (a barrier
+        // nothing targets, no time allowed) aborts every role of the CTA.
+        if (tid == 0 && !mbar_wait_ns(mma_done + 1, 0, 0)) raise_abort(abort_flag, a.dev_status);
+        __syncthreads();
+    }
 
     if (warp == kProducerWarp) {
         // ================================ producer ================================
         const int xc = a.head_first ? g : 0, yc = a.head_first ? 0 : g;
-        if (lane == 0) {
+        const bool q_issued = !*abort_flag;
+        if (lane == 0 && q_issued) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(dst + hh * kHalfBytes + lane * P * 128, map, bar, 64 * hh, xc, yc, pg);
         };
         int kq = 0, vq = 0;  // tiles issued
-        bool ok = true;
+        bool ok = q_issued;
         for (int j = 0; ok && j < nt; ++j) {
             // physical page of lane's slot in tile j (out-of-pool entries flagged, read as zeros)
             int pg = a.num_pages;  // beyond the tensor: the box reads as zeros
@@ -299,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // never leave the CTA with copies in flight
             for (int j = max(0, kq - kKS); j < kq; ++j) mbar_wait_ns(&k_full[j % kKS], (j / kKS) & 1, kWaitNs);
             for (int j = max(0, vq - kVS); j < vq; ++j) mbar_wait_ns(&v_full[j % kVS], (j / kVS) & 1, kWaitNs);
-            if (!mbar_wait_ns(q_full, 0, kWaitNs)) flag(a.dev_status, PA_DEV_TIMEOUT);
+            if (q_issued && !mbar_wait_ns(q_full, 0, kWaitNs)) flag(a.dev_status, PA_DEV_TIMEOUT);
         }
     } else if (warp == kMmaWarp) {
         // ================================== MMA ===================================
@@ -645,6 +654,7 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cuda
     p.max_q_len = a.max_q_len;
     p.total_q = a.total_q;
     p.B = a.num_seqs;
+    p.debug_timeout = a.debug_timeout;
     p.head_first = head_first;
     p.scale_log2 = a.scale_log2;
     const int64_t n_pairs = (a.max_q_len + 2 * tq - 1) / (2 * tq);  // pairs of row tiles

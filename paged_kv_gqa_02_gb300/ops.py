@@ -45,7 +45,7 @@ class Params(ctypes.Structure):
                 ("out_dtype", ctypes.c_int32), ("deterministic", ctypes.c_int32),
                 ("num_splits", ctypes.c_int32), ("decode_phases", ctypes.c_int32),
                 ("decode_q_rows", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
-                ("single_launch", ctypes.c_int32)]
+                ("single_launch", ctypes.c_int32), ("debug_timeout", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -89,7 +89,7 @@ def load(path: str = LIB_PATH):
 def make_params(*, num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                 max_blocks_per_seq, max_context_len, scale=None, dtype="bf16", kv_dtype=None,
                 deterministic=1, num_splits=0, strides=(0, 0, 0), decode_phases=0,
-                decode_q_rows=0, sliding_window=0, single_launch=0) -> Params:
+                decode_q_rows=0, sliding_window=0, single_launch=0, debug_timeout=0) -> Params:
     p = Params()
     load().pa_params_init(ctypes.byref(p))
     p.num_seqs, p.num_q_heads, p.num_kv_heads = num_seqs, num_q_heads, num_kv_heads
@@ -105,6 +105,7 @@ def make_params(*, num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num
     p.decode_q_rows = decode_q_rows
     p.sliding_window = sliding_window
     p.single_launch = single_launch
+    p.debug_timeout = debug_timeout
     return p
 
 

@@ -46,6 +46,17 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.pa_build_flags() == 0  # the release build: no range checks compiled in
 
 
+def test_make_params_sets_every_field(lib):
+    """ops.make_params accepts and stores each optional pa_params field."""
+    kw = dict(deterministic=0, num_splits=3, strides=(4096, 1024, 128), decode_phases=1,
+              decode_q_rows=2, sliding_window=64, single_launch=1, debug_timeout=1)
+    p = ops.make_params(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=32,
+                        num_pages=10, max_blocks_per_seq=4, max_context_len=128, **kw)
+    assert (p.page_stride, p.token_stride, p.head_stride) == kw.pop("strides")
+    for k, v in kw.items():
+        assert getattr(p, k) == v, k
+
+
 def test_params_struct_layout_matches_header(lib):
     """pa_params_init writes the defaults the header documents."""
     p = ops.Params()
@@ -109,7 +120,7 @@ def call_decode(p, q=FAKE, out=FAKE, bt=FAKE, ws=None, nbytes=0):
     ("kv_dtype", ops.PA_F16, 6), ("out_dtype", ops.PA_BF16, 6), ("deterministic", 2, 2),
     ("num_splits", -1, 2), ("head_stride", 4, 4), ("token_stride", 100, 4),
     ("decode_phases", 4, 2), ("decode_phases", -1, 2), ("single_launch", 2, 2),
-    ("single_launch", -1, 2),
+    ("single_launch", -1, 2), ("debug_timeout", 2, 2),
 ])
 def test_rejects_bad_params(lib, field, value, code):
     p = base_params()
