@@ -293,14 +293,14 @@ def time_graph(torch, calls, K, W, world):
     return e0.elapsed_time(e1), t0, t1
 
 
-def decode_calls(rot, ops, torch, partial_only=False, single=False):
-    """pa_decode calls over the rotation copies; with partial_only, the same
-    calls restricted to the partial kernel (decode_phases = 1); with single,
-    the single-launch form (single_launch = 1)."""
+def decode_calls(rot, ops, torch, partial_only=False, form=0):
+    """pa_decode calls over the rotation copies in decode form `form`
+    (PA_FORM_AUTO, PA_FORM_PAIR or PA_FORM_COUNTED); with partial_only, the
+    pair's partial kernel alone (decode_phases = 1)."""
     import copy
     p = copy.copy(rot.params)
     p.decode_phases = 1 if partial_only else 0
-    p.single_launch = 1 if single and not partial_only else 0
+    p.decode_form = ops.PA_FORM_PAIR if partial_only else form
     S, _ = ops.decode_plan(p)
     nws = ops.decode_workspace_size(p)
     ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device="cuda")
@@ -317,15 +317,17 @@ def decode_calls(rot, ops, torch, partial_only=False, single=False):
 
 
 def single_launch(p) -> bool:
-    """Whether pa_decode runs these parameters as one kernel: single_launch
-    asked for, 16-bit K/V, automatic splits, head_dim <= 128 and one MMA
-    column tile (query rows x q heads per kv head <= 8)."""
+    """Whether pa_decode runs these parameters as one kernel: the counted
+    form, 16-bit K/V, automatic splits, head_dim <= 128, one MMA column tile
+    (query rows x q heads per kv head <= 8)."""
     from paged_kv_gqa_02_gb300 import ops
     rows = max(1, p.decode_q_rows)
     g = p.num_q_heads // p.num_kv_heads
     rb = min(rows, (8 if p.head_dim == 256 else 16) // g)
-    return (p.single_launch == 1 and p.num_splits == 0 and p.kv_dtype != ops.PA_F32
-            and p.head_dim <= 128 and rb * g <= 8 and p.decode_phases in (0, 3))
+    if not (p.num_splits == 0 and p.kv_dtype != ops.PA_F32 and p.head_dim <= 128 and rb * g <= 8
+            and p.decode_phases in (0, 3)):
+        return False
+    return p.decode_form == ops.PA_FORM_COUNTED
 
 
 def append_calls(rot, wl, ops, torch):
@@ -528,14 +530,18 @@ def measure_workload(wl, ops, torch, K, W, world, l2, hbm_peak, flop_peak, clock
         if launches == 1:
             # one kernel per call: its average launch period is the call's,
             # and it moves every algorithmic byte (K/V, q and out)
-            dom_name, dom_ms, dom_bytes = "decode (single launch)", per_call, wl.algorithmic_bytes()
+            dom_name, dom_ms, dom_bytes = "decode (one kernel)", per_call, wl.algorithmic_bytes()
         else:
             dom_name, dom_ms, dom_bytes = "decode split partial", part, wl.kv_bytes() + wl.q_bytes()
         achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-        scalls, slaunches, _ = decode_calls(rot, ops, torch, single=True)
-        if slaunches == 1:
-            sms, _, _ = time_graph(torch, scalls, K, W, world)
-            res["single_launch_us_per_call"] = max_over_ranks(sms, world) / K * 1e3
+        for form, key in ((ops.PA_FORM_PAIR, "pair"), (ops.PA_FORM_COUNTED, "counted")):
+            fcalls, flaunches, _ = decode_calls(rot, ops, torch, form=form)
+            if form == ops.PA_FORM_PAIR and launches == 2:
+                continue  # the main measurement is the pair already
+            if form == ops.PA_FORM_COUNTED and flaunches != 1:
+                continue
+            fms, _, _ = time_graph(torch, fcalls, K, W, world)
+            res[f"{key}_us_per_call"] = max_over_ranks(fms, world) / K * 1e3
         ams, _, _ = time_graph(torch, append_calls(rot, wl, ops, torch), K, W, world)
         res["append_us_per_call"] = max_over_ranks(ams, world) / K * 1e3
         for T in (2, 4):
@@ -639,8 +645,8 @@ def run_ours(args):
                    "timing": "CUDA graph replays, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
         "decode_append_us_per_call": round(main["append_us_per_call"], 3) if "append_us_per_call" in main else None,
-        "decode_single_launch_us_per_call": round(main["single_launch_us_per_call"], 3)
-        if "single_launch_us_per_call" in main else None,
+        "decode_forms_us_per_call": {k: round(main[f"{k}_us_per_call"], 3) for k in ("pair", "counted")
+                                     if f"{k}_us_per_call" in main},
         "decode_rows_us_per_call": {T: round(main[f"rows{T}_us_per_call"], 3) for T in (2, 4)
                                     if f"rows{T}_us_per_call" in main},
         "decode_window1024": {"us_per_call": round(main["window1024_us_per_call"], 3),

@@ -65,6 +65,9 @@ typedef struct CUstream_st *pa_stream_t;
 
 typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 
+/* pa_params.decode_form */
+enum { PA_FORM_AUTO = 0, PA_FORM_PAIR = 1, PA_FORM_COUNTED = 2 };
+
 typedef enum {
     PA_OK = 0,
     PA_ERR_NULL = 1,        /* a required pointer is NULL                  */
@@ -139,13 +142,14 @@ typedef struct {
                                    pa_decode_append with 16-bit K/V and
                                    automatic splits only; otherwise
                                    PA_ERR_UNSUPPORTED.                            */
-    int32_t single_launch;      /* pa_decode / pa_decode_append: 1 = run the
-                                   call as one kernel where it can (16-bit K/V,
-                                   automatic splits, head_dim <= 128, rows x
-                                   Hq/Hkv <= 8): the split partial kernel also
-                                   merges the pieces (see pa_decode).  0 (the
-                                   default) = partial kernel + combine kernel,
-                                   the faster form on GB300.                     */
+    int32_t decode_form;        /* pa_decode / pa_decode_append with 16-bit K/V,
+                                   automatic splits, head_dim <= 128 and rows x
+                                   Hq/Hkv <= 8 (see pa_decode):
+                                   PA_FORM_AUTO (0, default): the library's
+                                   choice, today the partial + combine pair;
+                                   PA_FORM_PAIR (1): the pair; PA_FORM_COUNTED
+                                   (2): one kernel whose last CTA per unit
+                                   merges its pieces.  Other calls ignore it.   */
     int32_t debug_timeout;      /* testing only, 0 otherwise.  1: every wait of
                                    the split-KV decode kernel and of the tensor-
                                    core prefill kernel gives up at once, before
@@ -180,6 +184,13 @@ const char *pa_status_string(pa_status s);
  * *split_tokens = keys per split.  Either output may be NULL. */
 pa_status pa_decode_plan(const pa_params *p, int32_t *num_splits, int32_t *split_tokens);
 
+/* Kernels one pa_decode call (with_append = 0) or pa_decode_append call
+ * (with_append = 1) launches for these parameters: 1 for the counted single
+ * launch and single-split calls, 2 for the partial + combine pair, 3 when
+ * the append needs its scatter kernel, and so on; -1 for invalid or
+ * unsupported parameters.  For callers that budget graph nodes. */
+int32_t pa_decode_kernels(const pa_params *p, int32_t with_append);
+
 /* Bytes of workspace pa_decode needs for these parameters (0 on the fixed
  * split path when the plan has a single split).  Returns 0 for invalid
  * parameters. */
@@ -204,14 +215,13 @@ size_t pa_decode_workspace_size(const pa_params *p);
  * ascending share order:
  *  - by a second kernel, launched with programmatic dependent launch so that
  *    its CTAs are resident and have located their pieces when the partial
- *    kernel ends (the default);
- *  - with single_launch = 1, head_dim <= 128 and rows x Hq/Hkv <= 8 (one MMA
- *    column tile), in the partial kernel itself: each CTA merges its warps'
- *    pieces, and the last CTA to leave a piece of a unit (counted on a
- *    workspace counter with an acquire-release atomic) merges the unit's CTA
- *    pieces.  One kernel per call; on GB300 it takes longer than the pair,
- *    because the count and the finishing CTA's reads sit on the critical
- *    path after the slowest CTA.
+ *    kernel ends (PA_FORM_AUTO and PA_FORM_PAIR);
+ *  - PA_FORM_COUNTED, head_dim <= 128 and rows x Hq/Hkv <= 8: in the partial
+ *    kernel itself, each CTA merges its warps' pieces and the last CTA to
+ *    leave a piece of a unit (counted on a workspace counter with an
+ *    acquire-release atomic) merges the unit's CTA pieces.  One kernel; on
+ *    GB300 it takes longer than the pair, because the count and the
+ *    finishing CTA's reads sit on the critical path after the slowest CTA.
  * Otherwise the fixed split plan of pa_decode_plan is used (the
  * pa_decode_partial + pa_combine pair). */
 #define PA_DECODE_COUNTER_BYTES 4096u

@@ -51,7 +51,7 @@ pa_status check_params(const pa_params* p, Resolved* r) {
     if (p->decode_q_rows < 0 || p->decode_q_rows > kMaxDecodeRows) return PA_ERR_SHAPE;
     if (p->decode_q_rows > p->max_context_len) return PA_ERR_SHAPE;
     if (p->sliding_window < 0) return PA_ERR_SHAPE;
-    if (p->single_launch != 0 && p->single_launch != 1) return PA_ERR_SHAPE;
+    if (p->decode_form < PA_FORM_AUTO || p->decode_form > PA_FORM_COUNTED) return PA_ERR_SHAPE;
     if (p->debug_timeout != 0 && p->debug_timeout != 1) return PA_ERR_SHAPE;
     const int64_t D = p->head_dim;
     r->head_stride = p->head_stride ? p->head_stride : D;
@@ -280,6 +280,35 @@ PA_EXPORT pa_status pa_combine(const pa_params* p, const float* partial_ml,
 }
 
 namespace {
+// The split-KV kernel's call for these parameters, pointers left NULL.
+pa::DecodeV1Call v1_call(const pa_params* p, const Resolved& r) {
+    pa::DecodeV1Call c;
+    memset(&c, 0, sizeof c);
+    c.dtype = p->kv_dtype;
+    c.B = p->num_seqs;
+    c.Hq = p->num_q_heads;
+    c.Hkv = p->num_kv_heads;
+    c.D = p->head_dim;
+    c.P = p->page_size;
+    c.num_pages = p->num_pages;
+    c.max_blocks = p->max_blocks_per_seq;
+    c.n_ctas = v1_ctas(p);
+    c.page_stride = r.page_stride;
+    c.token_stride = r.token_stride;
+    c.head_stride = r.head_stride;
+    c.scale_log2 = p->scale * pa::kLog2e;
+    c.phases = p->decode_phases ? p->decode_phases : 3;
+    c.rows = decode_rows(p);
+    c.window = p->sliding_window;
+    c.row0 = 0;
+    c.row_count = c.rows;
+    c.row_block = row_block(p);  // blocks of rows are units of one launch
+    c.single_launch = p->decode_form == PA_FORM_COUNTED;
+    c.max_context_len = p->max_context_len;
+    c.debug_timeout = p->debug_timeout;
+    return c;
+}
+
 // pa_decode, with the new token's K/V appended first when k_new is set.
 pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, const void* v_new,
                       const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -301,7 +330,7 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         if (!workspace) return PA_ERR_NULL;
         if (workspace_bytes < need) return PA_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_ALIGN;
-        pa::DecodeV1Call c;
+        pa::DecodeV1Call c = v1_call(p, r);
         c.q = q;
         c.k = k_cache;
         c.v = v_cache;
@@ -310,30 +339,8 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
         c.out = out;
         c.workspace = workspace;
         c.dev_status = dev_status;
-        c.dtype = p->kv_dtype;
-        c.B = p->num_seqs;
-        c.Hq = p->num_q_heads;
-        c.Hkv = p->num_kv_heads;
-        c.D = p->head_dim;
-        c.P = p->page_size;
-        c.num_pages = p->num_pages;
-        c.max_blocks = p->max_blocks_per_seq;
-        c.n_ctas = n;
-        c.page_stride = r.page_stride;
-        c.token_stride = r.token_stride;
-        c.head_stride = r.head_stride;
-        c.scale_log2 = p->scale * pa::kLog2e;
-        c.phases = p->decode_phases ? p->decode_phases : 3;
-        c.rows = rows;
-        c.window = p->sliding_window;
         c.k_new = k_new;  // fused: the partial kernel writes and attends the new rows
         c.v_new = v_new;
-        c.row0 = 0;
-        c.row_count = rows;
-        c.row_block = rb;  // blocks of rows are units of one launch
-        c.single_launch = p->single_launch;
-        c.max_context_len = p->max_context_len;
-        c.debug_timeout = p->debug_timeout;
         return cuda_status(pa::launch_decode_v1(c, stream));
     }
     if (p->sliding_window > 0) return PA_ERR_UNSUPPORTED;  // windows: split-KV kernel only
@@ -401,6 +408,24 @@ pa_status decode_impl(const pa_params* p, const void* q, const void* k_new, cons
                                              p->num_q_heads, S, p->head_dim, stream));
 }
 }  // namespace
+
+PA_EXPORT int32_t pa_decode_kernels(const pa_params* p, int32_t with_append) {
+    Resolved r;
+    if (check_params(p, &r) != PA_OK || d256_unsupported(p)) return -1;
+    const int phases = p->decode_phases ? p->decode_phases : 3;
+    if (use_v1(p)) {
+        pa::DecodeV1Call c = v1_call(p, r);
+        if (with_append) c.k_new = c.v_new = &c;  // only marks the append (the plan has no small-call form for it)
+        return pa::decode_v1_kernels(c);
+    }
+    if (p->sliding_window > 0 || (with_append && decode_rows(p) > 1)) return -1;
+    int S, tok;
+    plan(p, &S, &tok);
+    if (decode_rows(p) > 1 && !rows_split_ok(p)) S = 1;
+    const int scatter = with_append && (phases & 1) ? 1 : 0;  // the append's scatter kernel
+    if (S == 1) return (phases & 1) ? 1 + scatter : 0;
+    return ((phases & 1) ? 1 + scatter : 0) + ((phases & 2) ? 1 : 0);
+}
 
 PA_EXPORT pa_status pa_decode(const pa_params* p, const void* q, const void* k_cache,
                               const void* v_cache, const int32_t* block_tables,

@@ -319,7 +319,7 @@ __device__ inline int warps_in_use(long long T, long long n_cta) {
 // thread of the CTA takes (head, 4 dims) items; the pieces are read through
 // L2 (ld.global.cg) in batches whose loads are all in flight together.
 template <int D>
-__device__ inline void finish_unit(const V1Params& a, int u, int c0, int np) {
+__device__ __noinline__ void finish_unit(const V1Params& a, int u, int c0, int np) {
     constexpr int kB = 16;  // pieces loaded together
     const int G = a.G, ub = u / a.Hv, ug = u % a.Hv, Gu = unit_cols(a, ug);
     for (int idx = threadIdx.x; idx < G * D / 4; idx += kThreadsV1) {
@@ -432,7 +432,8 @@ __global__ void __maxnreg__(224)
     __shared__ long long s_p0[kCW][2];  // CTA merge: cost position of the unit's first page
     __shared__ int s_pb[kCW][2];        // and its page count
     __shared__ int4 s_run[2 * kCW];     // CTA merge: (unit, entry mask, inside, first entry) of each run
-    __shared__ int s_nruns;
+    __shared__ float s_w[kCtaMerge ? 8 : 1][2 * kCW];  // CTA merge: weight of each entry, per head
+    __shared__ float s_md[kCtaMerge ? 8 : 1][2];       // CTA merge: max and denominator, per head
     __shared__ __align__(8) uint64_t s_never;  // a barrier no copy or thread ever arrives on (debug_timeout)
     __shared__ int2 s_fin[2 * kCW];     // single launch: (unit, first CTA) of each run this CTA completes
     __shared__ int s_fnp[2 * kCW];      // and its CTA pieces
@@ -583,8 +584,6 @@ __global__ void __maxnreg__(224)
     // stays in o / mrun / lrun.
     float of[kKs][4], mf[2], lf[2];
     int first_unit = -1, first_inside = 0, last_unit = -1, last_inside = 0;
-    long long first_p0 = 0, last_p0 = 0;  // cost position of the piece's unit's first page
-    int first_pb = 0, last_pb = 0;       // and its pages
     float mrun[NT][2], lrun[NT][2];
 
     while (!wk.done) {
@@ -827,8 +826,10 @@ __global__ void __maxnreg__(224)
                 if (!nx.done) {  // the share's first piece; later units follow
                     first_unit = unit;
                     first_inside = inside;
-                    first_p0 = p0;
-                    first_pb = wk.pb;
+                    if (lane == 0) {  // where the unit's pages sit (the counted single launch)
+                        s_p0[warp][0] = p0;
+                        s_pb[warp][0] = wk.pb;
+                    }
 #pragma unroll
                     for (int dt = 0; dt < kKs; ++dt)
 #pragma unroll
@@ -840,8 +841,10 @@ __global__ void __maxnreg__(224)
                 } else {
                     last_unit = unit;
                     last_inside = inside;
-                    last_p0 = p0;
-                    last_pb = wk.pb;
+                    if (lane == 0) {
+                        s_p0[warp][1] = p0;
+                        s_pb[warp][1] = wk.pb;
+                    }
                 }
             }
         } else {
@@ -910,85 +913,89 @@ __global__ void __maxnreg__(224)
         if (lane == 0) {
             s_unit[warp][0] = first_unit;
             s_inside[warp][0] = first_inside;
-            s_p0[warp][0] = first_p0;
-            s_pb[warp][0] = first_pb;
             s_unit[warp][1] = last_unit;
             s_inside[warp][1] = last_inside;
-            s_p0[warp][1] = last_p0;
-            s_pb[warp][1] = last_pb;
         }
         __syncthreads();
-        // Entries f = 0 .. 15 (warp f / 2, first then last piece) are in cost
-        // order, and a unit's entries are consecutive: a run is a maximal group
-        // of valid entries of one unit.  Warp 0 lists the runs; then every
-        // thread takes (run, head, 4 dims) items and merges the run's entries in
-        // ascending order, all loads of an item in flight together.  A unit
-        // whose pages all lie in this CTA's share is finished here; the others
-        // leave one piece (slot CTA + unit).
-        if (warp == 0) {
-            const int f = lane & (2 * kCW - 1);
-            const int su = s_unit[f >> 1][f & 1];
-            const uint32_t vmask = __ballot_sync(0xffffffffu, su >= 0) & 0xffffu;
-            const uint32_t lower = vmask & ((1u << f) - 1u);
-            const int pu = __shfl_sync(0xffffffffu, su, lower ? 31 - __clz(lower) : 0);
-            const uint32_t starts = __ballot_sync(0xffffffffu, su >= 0 && (lower == 0 || pu != su)) & 0xffffu;
-            if (lane < 2 * kCW && ((starts >> f) & 1u)) {
-                const uint32_t above = starts & ~((2u << f) - 1u);
-                const int nxt = above ? __ffs(above) - 1 : 2 * kCW;
-                s_run[__popc(starts & ((1u << f) - 1u))] =
-                    make_int4(su, int(vmask & ((1u << nxt) - (1u << f))), s_inside[f >> 1][f & 1], f);
-            }
-            if (lane == 0) s_nruns = __popc(starts);
-        }
-        __syncthreads();
-        const int nruns = s_nruns;
-        const int per_run = G * (D / 4);
-        for (int it = threadIdx.x; it < nruns * per_run; it += kThreadsV1) {
-            const int r = it / per_run, rest = it - r * per_run;
-            const int h = rest / (D / 4), d4 = (rest % (D / 4)) * 4;
-            const int4 run = s_run[r];
-            const uint32_t emask = uint32_t(run.y);
-            float2 ml[2 * kCW];
-            float4 v[2 * kCW];
+        // Merge, unit by unit in warp order, the pieces that warps of this CTA
+        // share; a unit whose pages all lie in this CTA's share is finished
+        // here, the others leave one piece for the combine (slot CTA + unit).
+        // Every warp reads the 16 entry descriptors (lane f and f + 16 hold
+        // entry f) and finds, with ballots, where each unit's entries start and
+        // which entries hold it.  The code stays short: it runs once per CTA
+        // and launch, so its instructions are fetched cold.
+        const int f = lane & (2 * kCW - 1);
+        const int su = s_unit[f >> 1][f & 1];
+        const uint32_t vmask = __ballot_sync(0xffffffffu, su >= 0) & 0xffffu;
+        const uint32_t lower = vmask & ((1u << f) - 1u);
+        const int pu = __shfl_sync(0xffffffffu, su, lower ? 31 - __clz(lower) : 0);
+        const uint32_t starts = __ballot_sync(0xffffffffu, su >= 0 && (lower == 0 || pu != su)) & 0xffffu;
+        auto piece = [&](int ff) {
+            return reinterpret_cast<const float*>(base + size_t(ff >> 1) * NH * kTile) + (ff & 1) * pstride;
+        };
+        int k = 0;  // run index: the counted single launch finishes the runs that leave the CTA
+        for (uint32_t sm = starts; sm; sm &= sm - 1, ++k) {
+            const int e = __ffs(sm) - 1;
+            const int u = __shfl_sync(0xffffffffu, su, e);
+            const uint32_t emask = __ballot_sync(0xffffffffu, su == u) & 0xffffu;
+            const bool inside = s_inside[e >> 1][e & 1] != 0;
+            if (threadIdx.x == 0) s_run[k] = make_int4(u, int(emask), inside, e);
+            const int ub = u / a.Hv, ug = u % a.Hv;
+            // Weights: warp w takes heads 2w and 2w + 1, one lane per entry;
+            // maxima and denominators by fixed 16-lane shuffle trees.
+            if (2 * warp < G) {
+                const int h = 2 * warp + (lane >> 4);
+                const bool mine = h < G && ((emask >> f) & 1u);
+                const float mm = mine ? piece(f)[G * kRow + 2 * h] : -INFINITY;
+                const float ll = mine ? piece(f)[G * kRow + 2 * h + 1] : 0.f;
+                float M = mm;
 #pragma unroll
-            for (int ff = 0; ff < 2 * kCW; ++ff) {
-                const float* pc = reinterpret_cast<const float*>(base + size_t(ff >> 1) * NH * kTile) +
-                                  (ff & 1) * pstride;
-                if ((emask >> ff) & 1u) {
-                    ml[ff] = *reinterpret_cast<const float2*>(pc + G * kRow + 2 * h);
-                    v[ff] = *reinterpret_cast<const float4*>(pc + h * kRow + d4);
-                } else {
-                    ml[ff] = make_float2(-INFINITY, 0.f);
-                    v[ff] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                const float w = mm != -INFINITY ? ex2(mm - M) : 0.f;
+                float den = w * ll;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+                if (h < G) {
+                    s_w[h][f] = w;
+                    if (f == 0) {
+                        s_md[h][0] = M;
+                        s_md[h][1] = den;
+                    }
                 }
             }
-            float M = -INFINITY;
-#pragma unroll
-            for (int ff = 0; ff < 2 * kCW; ++ff) M = fmaxf(M, ml[ff].x);
-            float den = 0.f;
-            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int ff = 0; ff < 2 * kCW; ++ff) {
-                if (ml[ff].x == -INFINITY) continue;  // no entry, or no key: weight 0
-                const float w = ex2(ml[ff].x - M);
-                den = fmaf(w, ml[ff].y, den);
-                num.x = fmaf(w, v[ff].x, num.x);
-                num.y = fmaf(w, v[ff].y, num.y);
-                num.z = fmaf(w, v[ff].z, num.z);
-                num.w = fmaf(w, v[ff].w, num.w);
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < G * D / 4; idx += kThreadsV1) {
+                const int h = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
+                float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+                uint32_t m = emask;
+                while (m) {  // two entries a step, in ascending order
+                    const int f0 = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int f1 = m ? __ffs(m) - 1 : f0;
+                    const float w0 = s_w[h][f0], w1 = m ? s_w[h][f1] : 0.f;
+                    const float4 v0 = *reinterpret_cast<const float4*>(piece(f0) + h * kRow + d4);
+                    const float4 v1 = *reinterpret_cast<const float4*>(piece(f1) + h * kRow + d4);
+                    if (m) m &= m - 1;
+                    num.x = fmaf(w1, v1.x, fmaf(w0, v0.x, num.x));
+                    num.y = fmaf(w1, v1.y, fmaf(w0, v0.y, num.y));
+                    num.z = fmaf(w1, v1.z, fmaf(w0, v0.z, num.z));
+                    num.w = fmaf(w1, v1.w, fmaf(w0, v0.w, num.w));
+                }
+                const float M = s_md[h][0], den = s_md[h][1];
+                if (inside) {
+                    const float inv = den > 0.f ? 1.f / den : 0.f;
+                    if (h < unit_cols(a, ug) && PA_IN(row_off<D>(a, ub, ug, h) / D, a.out_rows, a.dev_status))
+                        *reinterpret_cast<float4*>(a.out + row_off<D>(a, ub, ug, h) + d4) =
+                            make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+                } else if (PA_IN((long long)blockIdx.x + u, a.ws_slots, a.dev_status)) {
+                    const long long slot = (long long)blockIdx.x + u;
+                    *reinterpret_cast<float4*>(a.ws_acc + (slot * G + h) * D + d4) = num;
+                    if (d4 == 0) *reinterpret_cast<float2*>(a.ws_ml + (slot * G + h) * 2) = make_float2(M, den);
+                }
             }
-            const int u = run.x, ub = u / a.Hv, ug = u % a.Hv;
-            if (run.z) {
-                const float inv = den > 0.f ? 1.f / den : 0.f;
-                if (h < unit_cols(a, ug) && PA_IN(row_off<D>(a, ub, ug, h) / D, a.out_rows, a.dev_status))
-                    *reinterpret_cast<float4*>(a.out + row_off<D>(a, ub, ug, h) + d4) =
-                        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-            } else if (PA_IN((long long)blockIdx.x + u, a.ws_slots, a.dev_status)) {
-                const long long slot = (long long)blockIdx.x + u;
-                *reinterpret_cast<float4*>(a.ws_acc + (slot * G + h) * D + d4) = num;
-                if (d4 == 0) *reinterpret_cast<float2*>(a.ws_ml + (slot * G + h) * 2) = make_float2(M, den);
-            }
+            __syncthreads();  // s_w / s_md are reused by the next unit
         }
+        const int nruns = k;
         if (a.finish) {
             // Every CTA piece of this CTA is written (barrier); one thread per
             // run orders them before counting them on the unit's counter
@@ -1275,45 +1282,10 @@ size_t decode_v1_workspace_bytes(int B, int Hkv, int G, int NB, int D, int n_cta
 }
 
 
-cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
+// The kernel parameters of a call (all but the tensor maps).
+cudaError_t build_params(const DecodeV1Call& call, V1Params& a) {
     const int D = call.D, P = call.P;
-    const CUtensorMapDataType dt =
-        call.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    // The pool as a 4-d tensor (head_dim, kv head, slot, page), the two middle
-    // dimensions in stride order; the box is one page of one kv head, 64 dims
-    // (128 bytes, the swizzle span) at a time.
     const int head_first = call.head_stride <= call.token_stride;
-    CUtensorMap mk, mv;
-    cuuint64_t dims[4], strides[3];
-    cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
-    dims[0] = D;
-    dims[3] = cuuint64_t(call.num_pages);
-    strides[2] = cuuint64_t(call.page_stride) * 2;
-    if (head_first) {
-        dims[1] = call.Hkv;
-        dims[2] = P;
-        strides[0] = cuuint64_t(call.head_stride) * 2;
-        strides[1] = cuuint64_t(call.token_stride) * 2;
-        box[0] = 64; box[1] = 1; box[2] = P; box[3] = 1;
-    } else {
-        dims[1] = P;
-        dims[2] = call.Hkv;
-        strides[0] = cuuint64_t(call.token_stride) * 2;
-        strides[1] = cuuint64_t(call.head_stride) * 2;
-        box[0] = 64; box[1] = P; box[2] = 1; box[3] = 1;
-    }
-    if (enc(&mk, dt, 4, const_cast<void*>(call.k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    if (enc(&mv, dt, 4, const_cast<void*>(call.v), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-
-    V1Params a;
     a.q = call.q;
     a.block_tables = call.block_tables;
     a.context_lens = call.context_lens;
@@ -1374,6 +1346,57 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     // at least one page tile per warp (head_dim 256 with 32-slot pages has
     // one: its K and V copies then take turns in it)
     if (a.ntiles < kCW || call.n_ctas > kMaxCounters) return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+int decode_v1_kernels(const DecodeV1Call& call) {
+    V1Params a;
+    if (build_params(call, a) != cudaSuccess) return -1;
+    if (!(call.phases & 1)) return (call.phases & 2) && !a.finish ? 1 : 0;
+    return a.finish ? 1 : ((call.phases & 2) ? 2 : 1);
+}
+
+cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int D = call.D, P = call.P;
+    const CUtensorMapDataType dt =
+        call.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // The pool as a 4-d tensor (head_dim, kv head, slot, page), the two middle
+    // dimensions in stride order; the box is one page of one kv head, 64 dims
+    // (128 bytes, the swizzle span) at a time.
+    const int head_first = call.head_stride <= call.token_stride;
+    CUtensorMap mk, mv;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+    dims[0] = D;
+    dims[3] = cuuint64_t(call.num_pages);
+    strides[2] = cuuint64_t(call.page_stride) * 2;
+    if (head_first) {
+        dims[1] = call.Hkv;
+        dims[2] = P;
+        strides[0] = cuuint64_t(call.head_stride) * 2;
+        strides[1] = cuuint64_t(call.token_stride) * 2;
+        box[0] = 64; box[1] = 1; box[2] = P; box[3] = 1;
+    } else {
+        dims[1] = P;
+        dims[2] = call.Hkv;
+        strides[0] = cuuint64_t(call.token_stride) * 2;
+        strides[1] = cuuint64_t(call.head_stride) * 2;
+        box[0] = 64; box[1] = P; box[2] = 1; box[3] = 1;
+    }
+    if (enc(&mk, dt, 4, const_cast<void*>(call.k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (enc(&mv, dt, 4, const_cast<void*>(call.v), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    V1Params a;
+    cudaError_t pe = build_params(call, a);
+    if (pe != cudaSuccess) return pe;
     const bool bf = call.dtype == PA_BF16;
 #define PA_V1_CASE(DD, PP)                                                                        \
     if (D == DD && P == PP)                                                                       \

@@ -63,5 +63,7 @@ cudaError_t launch_append_kv(const void* k_new, const void* v_new, void* k_cache
 // its first PA_DECODE_COUNTER_BYTES hold the single launch's arrival counters.
 size_t decode_v1_workspace_bytes(int B, int Hkv, int G, int NB, int D, int n_ctas);
 cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st);
+// Kernels launch_decode_v1 would launch for this call (1 or 2; -1: invalid).
+int decode_v1_kernels(const DecodeV1Call& call);
 
 }  // namespace pa

@@ -18,13 +18,14 @@ LIB_PATH = os.environ.get("PA_GQA_LIB") or os.path.join(PKG, "libpaged_gqa.so")
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 DTYPE_CODE = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16}
 PA_DEV_BAD_PAGE, PA_DEV_BAD_LEN, PA_DEV_TIMEOUT, PA_DEV_OOB = 1, 2, 4, 8
+PA_FORM_AUTO, PA_FORM_PAIR, PA_FORM_COUNTED = 0, 1, 2
 STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_DTYPE",
           4: "PA_ERR_ALIGN", 5: "PA_ERR_WORKSPACE", 6: "PA_ERR_UNSUPPORTED", 7: "PA_ERR_CUDA"}
 
 EXPORTS = ("pa_params_init", "pa_status_string", "pa_decode_plan", "pa_decode_workspace_size",
            "pa_decode", "pa_decode_partial", "pa_combine", "pa_prefill_workspace_size",
            "pa_prefill_chunk", "pa_version", "pa_decode_append", "pa_decode_noalloc",
-           "pa_build_flags")
+           "pa_build_flags", "pa_decode_kernels")
 
 
 class PaError(RuntimeError):
@@ -45,7 +46,7 @@ class Params(ctypes.Structure):
                 ("out_dtype", ctypes.c_int32), ("deterministic", ctypes.c_int32),
                 ("num_splits", ctypes.c_int32), ("decode_phases", ctypes.c_int32),
                 ("decode_q_rows", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
-                ("single_launch", ctypes.c_int32), ("debug_timeout", ctypes.c_int32)]
+                ("decode_form", ctypes.c_int32), ("debug_timeout", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -77,11 +78,15 @@ def load(path: str = LIB_PATH):
             L.pa_prefill_workspace_size.restype = sz
             L.pa_prefill_chunk.argtypes = [P, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             L.pa_decode_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+            if hasattr(L, "pa_decode_kernels"):
+                L.pa_decode_kernels.argtypes = [P, i32]
+                L.pa_decode_kernels.restype = i32
             for name in ("pa_decode_plan", "pa_decode", "pa_decode_append", "pa_decode_partial",
                          "pa_combine", "pa_prefill_chunk", "pa_decode_noalloc"):
                 getattr(L, name).restype = ctypes.c_int
             L.pa_version.restype = i32
-            L.pa_build_flags.restype = i32
+            if hasattr(L, "pa_build_flags"):
+                L.pa_build_flags.restype = i32
             _lib = L
     return _lib
 
@@ -89,7 +94,7 @@ def load(path: str = LIB_PATH):
 def make_params(*, num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                 max_blocks_per_seq, max_context_len, scale=None, dtype="bf16", kv_dtype=None,
                 deterministic=1, num_splits=0, strides=(0, 0, 0), decode_phases=0,
-                decode_q_rows=0, sliding_window=0, single_launch=0, debug_timeout=0) -> Params:
+                decode_q_rows=0, sliding_window=0, decode_form=0, debug_timeout=0) -> Params:
     p = Params()
     load().pa_params_init(ctypes.byref(p))
     p.num_seqs, p.num_q_heads, p.num_kv_heads = num_seqs, num_q_heads, num_kv_heads
@@ -104,7 +109,7 @@ def make_params(*, num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num
     p.decode_phases = decode_phases
     p.decode_q_rows = decode_q_rows
     p.sliding_window = sliding_window
-    p.single_launch = single_launch
+    p.decode_form = decode_form
     p.debug_timeout = debug_timeout
     return p
 
@@ -140,6 +145,11 @@ def decode_plan(p: Params):
     _check(load().pa_decode_plan(ctypes.byref(p), ctypes.byref(S), ctypes.byref(tok)),
            "pa_decode_plan")
     return S.value, tok.value
+
+
+def decode_kernels(p: Params, with_append: bool = False) -> int:
+    """Kernels one pa_decode (or pa_decode_append) call launches (-1: invalid)."""
+    return int(load().pa_decode_kernels(ctypes.byref(p), int(with_append)))
 
 
 def decode_workspace_size(p: Params) -> int:

@@ -49,7 +49,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_make_params_sets_every_field(lib):
     """ops.make_params accepts and stores each optional pa_params field."""
     kw = dict(deterministic=0, num_splits=3, strides=(4096, 1024, 128), decode_phases=1,
-              decode_q_rows=2, sliding_window=64, single_launch=1, debug_timeout=1)
+              decode_q_rows=2, sliding_window=64, decode_form=2, debug_timeout=1)
     p = ops.make_params(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=32,
                         num_pages=10, max_blocks_per_seq=4, max_context_len=128, **kw)
     assert (p.page_stride, p.token_stride, p.head_stride) == kw.pop("strides")
@@ -119,8 +119,8 @@ def call_decode(p, q=FAKE, out=FAKE, bt=FAKE, ws=None, nbytes=0):
     ("max_context_len", 16 * 32 + 1, 2), ("num_pages", 0, 2), ("q_dtype", 9, 3),
     ("kv_dtype", ops.PA_F16, 6), ("out_dtype", ops.PA_BF16, 6), ("deterministic", 2, 2),
     ("num_splits", -1, 2), ("head_stride", 4, 4), ("token_stride", 100, 4),
-    ("decode_phases", 4, 2), ("decode_phases", -1, 2), ("single_launch", 2, 2),
-    ("single_launch", -1, 2), ("debug_timeout", 2, 2),
+    ("decode_phases", 4, 2), ("decode_phases", -1, 2), ("decode_form", 3, 2),
+    ("decode_form", -1, 2), ("debug_timeout", 2, 2),
 ])
 def test_rejects_bad_params(lib, field, value, code):
     p = base_params()

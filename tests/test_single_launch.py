@@ -1,5 +1,5 @@
-"""Single-launch decode (pa_params.single_launch = 1): the split-KV kernel
-finishes every unit itself.
+"""Counted single-launch decode (pa_params.decode_form = PA_FORM_COUNTED):
+the split-KV kernel finishes every unit itself.
 
 16-bit K/V with automatic splits, head_dim <= 128 and at most 8 MMA columns
 (query rows x q heads per kv head) then run pa_decode as one kernel: each CTA
@@ -44,7 +44,7 @@ def _params(inp, meta, **kw):
                 page_size=meta["page_size"], num_pages=int(inp["num_pages"]),
                 max_blocks_per_seq=bt.shape[1], max_context_len=bt.shape[1] * meta["page_size"],
                 scale=meta["scale"], dtype=meta["q_dtype"], kv_dtype=meta["kv_dtype"],
-                single_launch=1)
+                decode_form=ops.PA_FORM_COUNTED)
     args.update(kw)
     return ops.make_params(**args)
 
@@ -74,6 +74,21 @@ SHAPES = [
 ]
 
 
+def test_kernels_per_call():
+    """pa_decode_kernels: the counted form is one kernel, the pair two, a
+    single-split fixed plan one, and the fp32 append adds its scatter."""
+    inp, meta = problem(B=2, Hq=32, Hkv=8, D=128, P=32, lens=(3000, 40), dt="bf16", num_pages=100, seed=3)
+    assert ops.decode_kernels(_params(inp, meta)) == 1
+    for form in (ops.PA_FORM_AUTO, ops.PA_FORM_PAIR):
+        assert ops.decode_kernels(_params(inp, meta, decode_form=form)) == 2
+    assert ops.decode_kernels(_params(inp, meta, decode_phases=1)) == 1
+    assert ops.decode_kernels(_params(inp, meta, num_splits=1)) == 1
+    assert ops.decode_kernels(_params(inp, meta, num_splits=4)) == 2
+    f32, m32 = problem(B=2, Hq=8, Hkv=2, D=64, P=16, lens=(300, 40), dt="f32", num_pages=30, seed=4)
+    assert ops.decode_kernels(_params(f32, m32), with_append=True) == 3
+    assert ops.decode_kernels(_params(inp, meta, head_dim=96)) == -1
+
+
 def test_one_workspace_serves_every_shape_and_counters_stay_zero():
     """One zeroed buffer, calls of different sizes in turn: each result
     matches the oracle, and the counter block is zero after every call."""
@@ -95,7 +110,7 @@ def test_one_workspace_serves_every_shape_and_counters_stay_zero():
 
 def test_single_launch_matches_the_two_kernel_form():
     """decode_phases 1 then 2 (partial kernel, then combine kernel) and the
-    single launch agree within the decode tolerance and both match the
+    counted single launch agree within the decode tolerance and both match the
     oracle; the single launch is bit-identical run to run."""
     for i, (B, Hq, Hkv, D, P, lens, dt) in enumerate(SHAPES[:3]):
         npages = sum((L + P - 1) // P for L in lens) + 5

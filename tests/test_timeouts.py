@@ -45,14 +45,14 @@ def _params(inp, meta, **kw):
     return ops.make_params(**args)
 
 
-@pytest.mark.parametrize("single", [0, 1])
-def test_decode_timeout_then_a_normal_call(single):
+@pytest.mark.parametrize("form", [0, 1, 2])
+def test_decode_timeout_then_a_normal_call(form):
     lens = (1, 31, 33, 700, 2500, 90)
     inp, meta = problem(B=6, Hq=32, Hkv=8, D=128, P=32, lens=lens, dt="bf16", num_pages=120, seed=5)
     d = ops.device_inputs(inp, "bf16")
     ws = torch.zeros(ops.decode_workspace_size(_params(inp, meta)), dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    p = _params(inp, meta, single_launch=single, debug_timeout=1)
+    p = _params(inp, meta, decode_form=form, debug_timeout=1)
     out = ops.decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
                      workspace=ws, dev_status=status)
     torch.cuda.synchronize()
@@ -60,7 +60,7 @@ def test_decode_timeout_then_a_normal_call(single):
     assert torch.isfinite(out).all()
     assert int(torch.count_nonzero(ws[:4096]).item()) == 0  # counters left at zero
     status.zero_()
-    p = _params(inp, meta, single_launch=single)
+    p = _params(inp, meta, decode_form=form)
     out = ops.decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
                      workspace=ws, dev_status=status)
     torch.cuda.synchronize()
