@@ -69,12 +69,38 @@ def peaks():
 _TOKENS = re.compile(r'"(?:\\.|[^"\\])*"' + r"|'(?:\\.|[^'\\])*'" + r"|//[^\n]*|/\*.*?\*/", re.S)
 
 
-def src_hash():
-    """Hash of the kernel sources without their comments and with runs of
-    white space collapsed: editing a comment leaves the compiled kernels, and
-    so the ncu counters taken on them, as they were."""
+# The translation unit each profiled kernel is compiled from.
+KERNEL_FILES = {"decode_v1": "pa_decode_v1.cu", "combine_v1": "pa_decode_v1.cu",
+                "prefill_tc": "pa_prefill_tc.cu", "decode_v0": "pa_tile_v0.cu", "combine_v0": "pa_tile_v0.cu"}
+_INCLUDE = re.compile(r'^\s*#\s*include\s+"([^"]+)"', re.M)
+
+
+def kernel_sources(kernel: str):
+    """The kernel's translation unit and every local header it includes,
+    directly or not (looked up beside the includer, then in include/)."""
+    csrc = os.path.join(ROOT, "paged_kv_gqa_02_gb300", "csrc")
+    todo, seen = [os.path.join(csrc, KERNEL_FILES[kernel])], []
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.append(f)
+        with open(f, encoding="utf-8") as fh:
+            for name in _INCLUDE.findall(fh.read()):
+                for d in (os.path.dirname(f), csrc, os.path.join(ROOT, "include")):
+                    if os.path.exists(os.path.join(d, name)):
+                        todo.append(os.path.join(d, name))
+                        break
+    return sorted(seen)
+
+
+def src_hash(kernel: str):
+    """Hash of the kernel's sources (kernel_sources) without their comments
+    and with runs of white space collapsed: editing a comment, or a file the
+    kernel does not include, leaves the compiled kernel, and so the ncu
+    counters taken on it, as they were."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "paged_kv_gqa_02_gb300", "csrc", "*"))):
+    for f in kernel_sources(kernel):
         with open(f, encoding="utf-8") as fh:
             text = fh.read()
         code = _TOKENS.sub(lambda m: " " if m.group(0).startswith("/") else m.group(0), text)
@@ -85,8 +111,10 @@ def src_hash():
 def read_traffic(workload: str, kernel: str):
     """Per-launch DRAM bytes from a committed ncu summary line of the form
     'bench-traffic: workload=W kernel=K bytes=N src=H scale=S', or None when
-    absent or taken on other kernel sources."""
-    cur = src_hash()
+    absent or taken on other sources of that kernel."""
+    if kernel not in KERNEL_FILES:
+        return None
+    cur = src_hash(kernel)
     for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for line in open(f):
             if not line.startswith("bench-traffic:"):

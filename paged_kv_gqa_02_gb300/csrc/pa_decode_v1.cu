@@ -86,7 +86,7 @@ struct V1Params {
     // (u / NB) * Gq + c % Gq.
     int32_t Tl, rb, NB, Hv;
     float scale_log2;
-    int32_t n_ctas, ntiles, head_first, unit_cost;
+    int32_t n_ctas, ntiles, unit_cost;
     int32_t cta_pieces;  // 1: the group fits one MMA column tile, so small calls merge per CTA
     // 1: single launch (asked for by the caller).  Every call merges its
     // warps' pieces per CTA, and the last CTA to leave a piece of a unit
@@ -523,12 +523,8 @@ __global__ void __maxnreg__(224)
             mbar_arrive_expect_tx(&my_full[slot], ok ? kTile : 0);
             if (ok) {
                 uint8_t* dst = my_tiles + size_t(slot) * kTile;
-                const int gh = unit_head(a, g);
-                const int xc = a.head_first ? gh : 0, yc = a.head_first ? 0 : gh;
-#pragma unroll
-                for (int hh = 0; hh < kHalves; ++hh)
-                    tma_load_4d_hint(dst + hh * P * 128, (hx & 1) ? &tmV : &tmK, &my_full[slot], 64 * hh, xc,
-                                     yc, pg, kv_policy);
+                tma_load_5d_hint(dst, (hx & 1) ? &tmV : &tmK, &my_full[slot], 0, 0, 0, unit_head(a, g), pg,
+                                 kv_policy);
             }
         }
         __syncwarp();
@@ -1285,7 +1281,6 @@ size_t decode_v1_workspace_bytes(int B, int Hkv, int G, int NB, int D, int n_cta
 // The kernel parameters of a call (all but the tensor maps).
 cudaError_t build_params(const DecodeV1Call& call, V1Params& a) {
     const int D = call.D, P = call.P;
-    const int head_first = call.head_stride <= call.token_stride;
     a.q = call.q;
     a.block_tables = call.block_tables;
     a.context_lens = call.context_lens;
@@ -1341,7 +1336,6 @@ cudaError_t build_params(const DecodeV1Call& call, V1Params& a) {
     a.token_stride = call.token_stride;
     a.head_stride = call.head_stride;
     a.ntiles = tile_count(D, P);
-    a.head_first = head_first;
     a.unit_cost = kUnitCost;
     // at least one page tile per warp (head_dim 256 with 32-slot pages has
     // one: its K and V copies then take turns in it)
@@ -1362,34 +1356,22 @@ cudaError_t launch_decode_v1(const DecodeV1Call& call, cudaStream_t st) {
     const int D = call.D, P = call.P;
     const CUtensorMapDataType dt =
         call.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    // The pool as a 4-d tensor (head_dim, kv head, slot, page), the two middle
-    // dimensions in stride order; the box is one page of one kv head, 64 dims
-    // (128 bytes, the swizzle span) at a time.
-    const int head_first = call.head_stride <= call.token_stride;
+    // The pool as a 5-d tensor (dim within a 64-dim half, slot, half, kv head,
+    // page), with each dimension's own stride: the box (64 x P x D/64 x 1 x 1)
+    // is one page of one kv head in one copy, and lands in shared memory as
+    // D/64 blocks of P rows of 128 bytes (the swizzle span), the layout the
+    // ldmatrix offsets assume.
     CUtensorMap mk, mv;
-    cuuint64_t dims[4], strides[3];
-    cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
-    dims[0] = D;
-    dims[3] = cuuint64_t(call.num_pages);
-    strides[2] = cuuint64_t(call.page_stride) * 2;
-    if (head_first) {
-        dims[1] = call.Hkv;
-        dims[2] = P;
-        strides[0] = cuuint64_t(call.head_stride) * 2;
-        strides[1] = cuuint64_t(call.token_stride) * 2;
-        box[0] = 64; box[1] = 1; box[2] = P; box[3] = 1;
-    } else {
-        dims[1] = P;
-        dims[2] = call.Hkv;
-        strides[0] = cuuint64_t(call.token_stride) * 2;
-        strides[1] = cuuint64_t(call.head_stride) * 2;
-        box[0] = 64; box[1] = P; box[2] = 1; box[3] = 1;
-    }
-    if (enc(&mk, dt, 4, const_cast<void*>(call.k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const cuuint64_t dims[5] = {64, cuuint64_t(P), cuuint64_t(D / 64), cuuint64_t(call.Hkv),
+                                cuuint64_t(call.num_pages)};
+    const cuuint64_t strides[4] = {cuuint64_t(call.token_stride) * 2, 128, cuuint64_t(call.head_stride) * 2,
+                                   cuuint64_t(call.page_stride) * 2};
+    const cuuint32_t box[5] = {64, cuuint32_t(P), cuuint32_t(D / 64), 1, 1}, estr[5] = {1, 1, 1, 1, 1};
+    if (enc(&mk, dt, 5, const_cast<void*>(call.k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (enc(&mv, dt, 4, const_cast<void*>(call.v), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (enc(&mv, dt, 5, const_cast<void*>(call.v), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;

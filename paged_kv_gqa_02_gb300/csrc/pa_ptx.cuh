@@ -104,6 +104,17 @@ __device__ inline void tma_load_4d_hint(void* dst, const CUtensorMap* map, uint6
         : "memory");
 }
 
+// A 5-d tile load with an L2 cache policy.
+__device__ inline void tma_load_5d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                        int c2, int c3, int c4, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // An L2 policy that marks lines as the first to evict: for data read once
 // (streamed K/V), so that it does not push out code and small hot tensors.
 __device__ inline uint64_t l2_policy_evict_first() {

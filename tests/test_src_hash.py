@@ -1,5 +1,6 @@
 """The kernel-source hash that ties committed ncu traffic figures to the
-sources they were taken on (bench.py): it ignores comments and white space,
+sources they were taken on (bench.py): it covers the kernel's translation
+unit and the local headers it includes, ignores comments and white space,
 follows every code change, and the committed decode summary's traffic line
 is well formed."""
 from __future__ import annotations
@@ -37,7 +38,19 @@ def test_committed_decode_summary_line_parses():
     lines = [x for x in open(path) if x.startswith("bench-traffic:")]
     assert len(lines) == 1
     kv = dict(x.split("=", 1) for x in lines[0].split()[1:])
-    assert kv["workload"] == "ragged_b16_32x8_d128" and kv["kernel"] == "decode_partial"
+    assert kv["workload"] == "ragged_b16_32x8_d128" and kv["kernel"] == "decode_v1"
     assert int(kv["bytes"]) > 110_000_000 and len(kv["src"]) == 12
-    got = bench.read_traffic("ragged_b16_32x8_d128", "decode_partial")
+    got = bench.read_traffic("ragged_b16_32x8_d128", "decode_v1")
     assert got is None or got == int(kv["bytes"]) * float(kv.get("scale", "1"))
+
+
+def test_kernel_sources_follow_includes():
+    """Each kernel's hash covers its own file and the headers it includes,
+    the public header among them, and no other kernel's file."""
+    names = lambda k: {os.path.basename(f) for f in bench.kernel_sources(k)}
+    dec, pre = names("decode_v1"), names("prefill_tc")
+    assert {"pa_decode_v1.cu", "pa_ptx.cuh", "pa_common.cuh", "paged_gqa.h"} <= dec
+    assert "pa_prefill_tc.cu" not in dec and "pa_tc.cuh" not in dec
+    assert {"pa_prefill_tc.cu", "pa_tc.cuh", "pa_ptx.cuh"} <= pre and "pa_decode_v1.cu" not in pre
+    assert bench.src_hash("decode_v1") != bench.src_hash("prefill_tc")
+    assert bench.read_traffic("ragged_b16_32x8_d128", "no_such_kernel") is None
