@@ -312,75 +312,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ================================== MMA ===================================
-        if (lane == 0) {
-            const uint32_t idQK = tc::idesc_f16(kBM, kBN, kBf16, false);
-            const uint32_t idPV = tc::idesc_f16(kBM, kD, kBf16, true);
-            const int nx = has_b ? 2 : 1;
-            bool ok = wait_bar(q_full, 0, abort_flag);
-            tc::fence_after_sync();
-            // descriptors: the high word is shared, low words advance by offset >> 4
-            const uint32_t hi_d = tc::desc_hi_sw128(1024);
-            const uint32_t q_lo = tc::desc_lo(smem_u32(sQ), 16);
-            const uint32_t k_lo = tc::desc_lo(smem_u32(k_tile(0)), 16);
-            const uint32_t v_lo = tc::desc_lo(smem_u32(v_tile(0)), kHalfBytes);
-            // S_x = Q_x K_j^T into the columns of tile x
-            auto qk = [&](int x, int j) {
-                const uint32_t qx = q_lo + x * (kTileBytes >> 4);
-                const uint32_t kx = k_lo + (j % kKS) * (kTileBytes >> 4);
+        // The whole warp runs this role, converged; one elected lane issues the
+        // MMAs and commits (the *_elect forms).  Issue from a lone lane in a
+        // divergent branch was measured at ~100 cycles an MMA once the softmax
+        // warps of the same sub-partition were busy, against the 64 cycles an
+        // MMA of this shape takes.
+        const uint32_t idQK = tc::idesc_f16(kBM, kBN, kBf16, false);
+        const uint32_t idPV = tc::idesc_f16(kBM, kD, kBf16, true);
+        const int nx = has_b ? 2 : 1;
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
+        };
+        bool ok = wait_all(q_full, 0);
+        tc::fence_after_sync();
+        // descriptors: the high word is shared, low words advance by offset >> 4
+        const uint32_t hi_d = tc::desc_hi_sw128(1024);
+        const uint32_t q_lo = tc::desc_lo(smem_u32(sQ), 16);
+        const uint32_t k_lo = tc::desc_lo(smem_u32(k_tile(0)), 16);
+        const uint32_t v_lo = tc::desc_lo(smem_u32(v_tile(0)), kHalfBytes);
+        // S_x = Q_x K_j^T into the columns of tile x
+        auto qk = [&](int x, int j) {
+            const uint32_t qx = q_lo + x * (kTileBytes >> 4);
+            const uint32_t kx = k_lo + (j % kKS) * (kTileBytes >> 4);
 #pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t off = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
-                    tc::mma_ss(tm + col_s(x), tc::make_desc(qx + off, hi_d), tc::make_desc(kx + off, hi_d), idQK,
-                               ks > 0);
-                }
-                tc::commit(&s_full[x]);
-            };
-            // O_x += P_x V_j, P_x read from the score columns of tile x
-            auto pv = [&](int x, int j) {
-                const uint32_t vx = v_lo + (j % kVS) * (kTileBytes >> 4);
-                const uint32_t p_col = tm + col_s(x), o_col = tm + col_o(x);
-#pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks) {
-                    // 16 keys: 8-row core groups 1024 B apart, dim halves 16 KB apart.
-                    // P of keys 32c..32c+31 sits in columns 32c (hi, 16) and 32c+16 (lo, 16).
-                    const uint64_t bd = tc::make_desc(vx + ks * (2048 >> 4), hi_d);
-                    const uint32_t col = p_col + 32 * (ks >> 1) + 8 * (ks & 1);
-                    tc::mma_ts(o_col, col, bd, idPV, j > 0 || ks > 0);
-                    tc::mma_ts(o_col, col + 16, bd, idPV, true);
-                }
-                tc::commit(&o_done[x]);
-            };
-            if (ok) ok = wait_bar(&k_full[0], 0, abort_flag);
-            if (ok) {
-                tc::fence_after_sync();
-                for (int x = 0; x < nx; ++x) qk(x, 0);
-                tc::commit(&k_empty[0]);
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint32_t off = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+                tc::mma_ss_elect(tm + col_s(x), tc::make_desc(qx + off, hi_d), tc::make_desc(kx + off, hi_d), idQK,
+                                 ks > 0);
             }
-            // per key tile and row tile x: P_x.V, then the next S_x, which
-            // overwrites P_x and so waits for that P.V to finish
-            for (int j = 0; ok && j < nt; ++j) {
-                for (int x = 0; ok && x < nx; ++x) {
-                    ok = wait_bar(&p_full[x], j & 1, abort_flag);
-                    if (ok && x == 0) ok = wait_bar(&v_full[j % kVS], (j / kVS) & 1, abort_flag);
+            tc::commit_elect(&s_full[x]);
+        };
+        // O_x += P_x V_j, P_x read from the score columns of tile x
+        auto pv = [&](int x, int j) {
+            const uint32_t vx = v_lo + (j % kVS) * (kTileBytes >> 4);
+            const uint32_t p_col = tm + col_s(x), o_col = tm + col_o(x);
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks) {
+                // 16 keys: 8-row core groups 1024 B apart, dim halves 16 KB apart.
+                // P of keys 32c..32c+31 sits in columns 32c (hi, 16) and 32c+16 (lo, 16).
+                const uint64_t bd = tc::make_desc(vx + ks * (2048 >> 4), hi_d);
+                const uint32_t col = p_col + 32 * (ks >> 1) + 8 * (ks & 1);
+                tc::mma_ts_elect(o_col, col, bd, idPV, j > 0 || ks > 0);
+                tc::mma_ts_elect(o_col, col + 16, bd, idPV, true);
+            }
+            tc::commit_elect(&o_done[x]);
+        };
+        if (ok) ok = wait_all(&k_full[0], 0);
+        if (ok) {
+            tc::fence_after_sync();
+            for (int x = 0; x < nx; ++x) qk(x, 0);
+            tc::commit_elect(&k_empty[0]);
+        }
+        // per key tile and row tile x: P_x.V, then the next S_x, which
+        // overwrites P_x and so waits for that P.V to finish
+        for (int j = 0; ok && j < nt; ++j) {
+            for (int x = 0; ok && x < nx; ++x) {
+                ok = wait_all(&p_full[x], j & 1);
+                if (ok && x == 0) ok = wait_all(&v_full[j % kVS], (j / kVS) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                pv(x, j);
+                if (x == nx - 1) tc::commit_elect(&v_empty[j % kVS]);
+                if (j + 1 < nt) {
+                    if (x == 0) ok = wait_all(&k_full[(j + 1) % kKS], ((j + 1) / kKS) & 1);
+                    if (ok) ok = wait_all(&o_done[x], j & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    pv(x, j);
-                    if (x == nx - 1) tc::commit(&v_empty[j % kVS]);
-                    if (j + 1 < nt) {
-                        if (x == 0) ok = wait_bar(&k_full[(j + 1) % kKS], ((j + 1) / kKS) & 1, abort_flag);
-                        if (ok) ok = wait_bar(&o_done[x], j & 1, abort_flag);
-                        if (!ok) break;
-                        tc::fence_after_sync();
-                        qk(x, j + 1);
-                        if (x == nx - 1) tc::commit(&k_empty[(j + 1) % kKS]);
-                    }
+                    qk(x, j + 1);
+                    if (x == nx - 1) tc::commit_elect(&k_empty[(j + 1) % kKS]);
                 }
             }
-            if (!ok) raise_abort(abort_flag, a.dev_status);
-            // every MMA issued so far has finished before tensor memory is freed
-            tc::commit(mma_done);
-            if (!mbar_wait_ns(mma_done, 0, kWaitNs)) flag(a.dev_status, PA_DEV_TIMEOUT);
         }
+        if (!ok && lane == 0) raise_abort(abort_flag, a.dev_status);
+        // every MMA issued so far has finished before tensor memory is freed
+        tc::commit_elect(mma_done);
+        if (!__all_sync(0xffffffffu, mbar_wait_ns(mma_done, 0, kWaitNs)) && lane == 0)
+            flag(a.dev_status, PA_DEV_TIMEOUT);
     } else if (warp < 4 || has_b) {
         // ================================= softmax =================================
         const int x = warp >> 2;  // tile
@@ -397,53 +404,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t obase = tm + lane_addr + col_o(x);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        uint32_t ra[32], rb[32];
+        // Table entry of page `lane` of key tile jj (0 for lanes past the
+        // tile's pages, which counts as a page inside the pool); loaded a key
+        // tile ahead of its use.
+        auto entry = [&](int jj) -> int {
+            const int idx = jj * PT + lane;
+            return lane < PT && idx < npg && PA_IN(idx, a.max_blocks, a.dev_status) ? __ldg(table + idx) : 0;
+        };
+        int e_cur = entry(0);
         for (int j = 0; j < nt; ++j) {
             const int k0 = j * kBN;
-            // pages of this tile outside the pool are skipped (flagged by the producer)
-            bool pok = true;
-            {
-                const int idx = j * PT + lane;
-                if (lane < PT && idx < npg && PA_IN(idx, a.max_blocks, a.dev_status)) {
-                    const int e = __ldg(table + idx);
-                    pok = e >= 0 && e < a.num_pages;
-                }
-            }
+            const int e_nxt = j + 1 < nt ? entry(j + 1) : 0;
             ok = __all_sync(0xffffffffu, wait_bar(&s_full[x], j & 1, abort_flag));
             if (!ok) break;
             tc::fence_after_sync();
-            const uint32_t pmask = __ballot_sync(0xffffffffu, pok);
+            // pages of this tile outside the pool are skipped (flagged by the producer)
+            const uint32_t pmask = __ballot_sync(0xffffffffu, e_cur >= 0 && e_cur < a.num_pages);
+            e_cur = e_nxt;
             const bool full = (k0 + kBN <= lim) && pmask == 0xffffffffu;
 
-            // ---- pass 1: row max of the raw scores (scale > 0 keeps the order)
+            // ---- pass 1: row max of the raw scores (scale > 0 keeps the order),
+            // 32 columns at a time.  Both passes are rolled loops: the code the
+            // softmax warps run stays small, so it does not push the MMA
+            // thread's code (same sub-partition) out of the instruction cache.
             float mx = -INFINITY;
-            tc::ld_32x32b_x32(sbase, ra);
-            tc::ld_32x32b_x32(sbase + 32, rb);
-            tc::wait_ld();
-            tc::reg_fence(ra);
-            tc::reg_fence(rb);
-#pragma unroll
-            for (int c = 0; c < 4; c += 2) {
-                if (!full) {
-                    apply_mask(ra, chunk_mask(lim - k0 - 32 * c, pmask, c, P));
-                    apply_mask(rb, chunk_mask(lim - k0 - 32 * (c + 1), pmask, c + 1, P));
-                }
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tc::ld_32x32b_x32(sbase + 32 * c, r);
+                tc::wait_ld();
+                tc::reg_fence(r);
+                if (!full) apply_mask(r, chunk_mask(lim - k0 - 32 * c, pmask, c, P));
                 float m0 = mx, m1 = -INFINITY;
 #pragma unroll
                 for (int k = 0; k < 32; k += 4) {
-                    m0 = max3(m0, __uint_as_float(ra[k]), __uint_as_float(ra[k + 1]));
-                    m1 = max3(m1, __uint_as_float(ra[k + 2]), __uint_as_float(ra[k + 3]));
-                    m0 = max3(m0, __uint_as_float(rb[k]), __uint_as_float(rb[k + 1]));
-                    m1 = max3(m1, __uint_as_float(rb[k + 2]), __uint_as_float(rb[k + 3]));
+                    m0 = max3(m0, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+                    m1 = max3(m1, __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
                 }
                 mx = fmaxf(m0, m1);
-                if (c == 0) {
-                    tc::ld_32x32b_x32(sbase + 64, ra);
-                    tc::ld_32x32b_x32(sbase + 96, rb);
-                    tc::wait_ld();
-                    tc::reg_fence(ra);
-                    tc::reg_fence(rb);
-                }
             }
             const float mt = mx * sl2;  // -inf when nothing is visible
             const bool need = mt > m_run + kRescaleStep;
@@ -455,48 +453,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             // issued after it)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                for (int c = 0; c < kD / 32; ++c) {
-                    tc::ld_32x32b_x32(obase + 32 * c, ra);
+                for (int c = 0; c < kD / 16; ++c) {
+                    uint32_t ro[16];
+                    tc::ld_32x32b_x16(obase + 16 * c, ro);
                     tc::wait_ld();
-                    tc::reg_fence(ra);
+                    tc::reg_fence(ro);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) ra[k] = __float_as_uint(__uint_as_float(ra[k]) * alpha);
-                    tc::st_32x32b_x32(obase + 32 * c, ra);
+                    for (int k = 0; k < 16; ++k) ro[k] = __float_as_uint(__uint_as_float(ro[k]) * alpha);
+                    tc::st_32x32b_x16(obase + 16 * c, ro);
                 }
             }
 
-            // ---- pass 2: p = 2^(s * scale_log2 - m_run), split hi + lo, written
-            // over the scores: keys 32c.. -> columns 32c (hi) and 32c + 16 (lo)
+            // ---- pass 2: p = 2^(s * scale_log2 - m_run), split hi + lo in place
+            // (hi over the even key of a pair, lo over the odd) and written over
+            // the scores: keys 32c.. -> columns 32c (hi) and 32c + 16 (lo)
             const float nmu = m_run == -INFINITY ? 0.f : -m_run;
             float sum0 = 0.f, sum1 = 0.f;
-            auto emit = [&](uint32_t (&r)[32], int c) {
-                uint32_t hi[16], lo[16];
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tc::ld_32x32b_x32(sbase + 32 * c, r);
+                tc::wait_ld();
+                tc::reg_fence(r);
+                if (!full) apply_mask(r, chunk_mask(lim - k0 - 32 * c, pmask, c, P));
 #pragma unroll
                 for (int w = 0; w < 16; ++w) {
                     const float p0 = ex2(fmaf(__uint_as_float(r[2 * w]), sl2, nmu));
                     const float p1 = ex2(fmaf(__uint_as_float(r[2 * w + 1]), sl2, nmu));
                     sum0 += p0;
                     sum1 += p1;
-                    Pack<T>::split(p0, p1, hi[w], lo[w]);
+                    Pack<T>::split(p0, p1, r[2 * w], r[2 * w + 1]);
                 }
-                tc::st_32x32b_x16(sbase + 32 * c, hi);
-                tc::st_32x32b_x16(sbase + 32 * c + 16, lo);
-            };
-            tc::ld_32x32b_x32(sbase, ra);
-            tc::wait_ld();
-            tc::reg_fence(ra);
-#pragma unroll 1
-            for (int c = 0; c < 4; c += 2) {
-                tc::ld_32x32b_x32(sbase + 32 * (c + 1), rb);
-                if (!full) apply_mask(ra, chunk_mask(lim - k0 - 32 * c, pmask, c, P));
-                emit(ra, c);
-                tc::wait_ld();
-                tc::reg_fence(rb);
-                if (c + 2 < 4) tc::ld_32x32b_x32(sbase + 32 * (c + 2), ra);
-                if (!full) apply_mask(rb, chunk_mask(lim - k0 - 32 * (c + 1), pmask, c + 1, P));
-                emit(rb, c + 1);
-                tc::wait_ld();
-                tc::reg_fence(ra);
+                tc::st_32x32b_x16_stride2<0>(sbase + 32 * c, r);
+                tc::st_32x32b_x16_stride2<1>(sbase + 32 * c + 16, r);
             }
             l_run += sum0 + sum1;
             tc::wait_st();
@@ -529,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* orow = a.out + (int64_t(row0 + r_tile + t) * a.Hq + g * G + h) * kD;
 #pragma unroll 1
             for (int c = 0; c < kD / 32; ++c) {
+                uint32_t ra[32];
                 tc::ld_32x32b_x32(obase + 32 * c, ra);
                 tc::wait_ld();
                 tc::reg_fence(ra);

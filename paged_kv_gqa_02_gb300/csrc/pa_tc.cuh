@@ -91,6 +91,40 @@ __device__ inline void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
         : "memory");
 }
 
+// The same two MMAs issued by one elected lane of a converged warp (the lowest
+// active lane, so always the same lane while the whole warp runs): the warp's
+// operands stay warp-uniform, and the issue needs no divergent branch.
+__device__ inline void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                    bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+__device__ inline void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                    bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+// commit() from the elected lane of a converged warp (the lane that issued
+// the MMAs through the *_elect forms).
+__device__ inline void commit_elect(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
 // Arrives on the mbarrier once all tcgen05 operations issued so far by this
 // thread have completed.
 __device__ inline void commit(uint64_t* bar) {
@@ -130,6 +164,29 @@ __device__ inline void st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
         "%14, %15, %16};" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ inline void ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Stores every other register of r (r[O], r[O + 2], ..., r[O + 30]) to 16
+// consecutive columns.
+template <int O>
+__device__ inline void st_32x32b_x16_stride2(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(r[O]), "r"(r[O + 2]), "r"(r[O + 4]), "r"(r[O + 6]), "r"(r[O + 8]), "r"(r[O + 10]), "r"(r[O + 12]),
+        "r"(r[O + 14]), "r"(r[O + 16]), "r"(r[O + 18]), "r"(r[O + 20]), "r"(r[O + 22]), "r"(r[O + 24]),
+        "r"(r[O + 26]), "r"(r[O + 28]), "r"(r[O + 30])
         : "memory");
 }
 
