@@ -110,24 +110,58 @@ __device__ inline float max3(float a, float b, float c) {
     return d;
 }
 
-// hi/lo split of two probabilities into packed 16-bit pairs (low half = even key)
+// Two fp32 values in one 64-bit register pair, and the paired fp32
+// arithmetic of sm_100-family cores (one instruction for both lanes, each
+// rounded as its scalar form).
+__device__ inline uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ inline void f2_unpack(uint64_t v, uint32_t& lo, uint32_t& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+__device__ inline uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ inline uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ inline uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// hi/lo split of two probabilities (a packed fp32 pair, low = even key) into
+// packed 16-bit pairs (low half = even key)
 template <typename T> struct Pack;
 template <> struct Pack<__nv_bfloat16> {
     // hi keeps the top 16 bits (truncation); lo = p - hi is exact in fp32 and
     // rounded to bf16, so hi + lo carries ~16 significant bits
-    __device__ static inline void split(float a, float b, uint32_t& hi, uint32_t& lo) {
-        const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+    __device__ static inline void split(uint64_t p, uint32_t& hi, uint32_t& lo) {
+        uint32_t ua, ub;
+        f2_unpack(p, ua, ub);
         hi = __byte_perm(ua, ub, 0x7632);
-        const __nv_bfloat162 l = __floats2bfloat162_rn(a - __uint_as_float(ua & 0xffff0000u),
-                                                       b - __uint_as_float(ub & 0xffff0000u));
+        uint32_t da, db;
+        f2_unpack(f2_sub(p, f2_pack(ua & 0xffff0000u, ub & 0xffff0000u)), da, db);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(__uint_as_float(da), __uint_as_float(db));
         lo = *reinterpret_cast<const uint32_t*>(&l);
     }
 };
 template <> struct Pack<__half> {
-    __device__ static inline void split(float a, float b, uint32_t& hi, uint32_t& lo) {
-        const __half2 h = __floats2half2_rn(a, b);
+    __device__ static inline void split(uint64_t p, uint32_t& hi, uint32_t& lo) {
+        uint32_t ua, ub;
+        f2_unpack(p, ua, ub);
+        const __half2 h = __floats2half2_rn(__uint_as_float(ua), __uint_as_float(ub));
         const float2 hf = __half22float2(h);
-        const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+        uint32_t da, db;
+        f2_unpack(f2_sub(p, f2_pack(__float_as_uint(hf.x), __float_as_uint(hf.y))), da, db);
+        const __half2 l = __floats2half2_rn(__uint_as_float(da), __uint_as_float(db));
         hi = *reinterpret_cast<const uint32_t*>(&h);
         lo = *reinterpret_cast<const uint32_t*>(&l);
     }
@@ -467,8 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- pass 2: p = 2^(s * scale_log2 - m_run), split hi + lo in place
             // (hi over the even key of a pair, lo over the odd) and written over
             // the scores: keys 32c.. -> columns 32c (hi) and 32c + 16 (lo)
+            // Key pairs go through the paired fp32 instructions: the scaled
+            // exponent, the two running sums (even and odd keys) and the lo
+            // remainder take one instruction a pair.
             const float nmu = m_run == -INFINITY ? 0.f : -m_run;
-            float sum0 = 0.f, sum1 = 0.f;
+            const uint64_t sl2_2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
+            const uint64_t nmu_2 = f2_pack(__float_as_uint(nmu), __float_as_uint(nmu));
+            uint64_t sum_2 = f2_pack(0u, 0u);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
@@ -478,16 +517,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!full) apply_mask(r, chunk_mask(lim - k0 - 32 * c, pmask, c, P));
 #pragma unroll
                 for (int w = 0; w < 16; ++w) {
-                    const float p0 = ex2(fmaf(__uint_as_float(r[2 * w]), sl2, nmu));
-                    const float p1 = ex2(fmaf(__uint_as_float(r[2 * w + 1]), sl2, nmu));
-                    sum0 += p0;
-                    sum1 += p1;
-                    Pack<T>::split(p0, p1, r[2 * w], r[2 * w + 1]);
+                    uint32_t z0, z1;
+                    f2_unpack(f2_fma(f2_pack(r[2 * w], r[2 * w + 1]), sl2_2, nmu_2), z0, z1);
+                    const uint64_t pp = f2_pack(__float_as_uint(ex2(__uint_as_float(z0))),
+                                                __float_as_uint(ex2(__uint_as_float(z1))));
+                    sum_2 = f2_add(sum_2, pp);
+                    Pack<T>::split(pp, r[2 * w], r[2 * w + 1]);
                 }
                 tc::st_32x32b_x16_stride2<0>(sbase + 32 * c, r);
                 tc::st_32x32b_x16_stride2<1>(sbase + 32 * c + 16, r);
             }
-            l_run += sum0 + sum1;
+            uint32_t sum0, sum1;
+            f2_unpack(sum_2, sum0, sum1);
+            l_run += __uint_as_float(sum0) + __uint_as_float(sum1);
             tc::wait_st();
 
             // slots past the context in its last page may hold anything (NaN):
