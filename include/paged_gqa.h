@@ -330,8 +330,8 @@ pa_status pa_decode_noalloc(const pa_params *p, const void *q, const void *k_cac
  * own K/V are already in the pages; row r attends keys 0 ..= L_s - T_s + r.
  * max_q_len is a host upper bound on every T_s (it sizes the grid);
  * total_q = cu_q_lens[B].  out is [total_q][Hq][D] f32.
- * For 16-bit Q/K/V with head_dim 128 and scale > 0 the work runs on the
- * tensor cores (tcgen05 MMA with tensor-memory accumulators); other
+ * For 16-bit Q/K/V with head_dim 64 or 128 and scale > 0 the work runs on
+ * the tensor cores (tcgen05 MMA with tensor-memory accumulators); other
  * supported shapes run on the CUDA cores.  No workspace is needed
  * (pa_prefill_workspace_size returns 0; workspace may be NULL). */
 size_t pa_prefill_workspace_size(const pa_params *p, int32_t total_q, int32_t max_q_len);

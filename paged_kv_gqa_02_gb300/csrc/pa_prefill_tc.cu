@@ -49,7 +49,6 @@ namespace pa {
 
 namespace {
 
-constexpr int kD = 128;          // head_dim served by this kernel
 constexpr int kBM = 128;         // MMA rows per row tile
 constexpr int kBN = 128;         // keys per tile
 constexpr int kKS = 3;           // K ring depth
@@ -57,22 +56,27 @@ constexpr int kVS = 2;           // V ring depth
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr uint32_t kTileBytes = kBN * kD * 2;  // one K (or V, or Q) tile
 constexpr uint32_t kHalfBytes = kBN * 128;     // one 64-dim half of a tile
-constexpr uint32_t kQOff = 0;                  // Q of A, then Q of B
-constexpr uint32_t kKOff = kQOff + 2 * kTileBytes;
-constexpr uint32_t kVOff = kKOff + kKS * kTileBytes;
-constexpr uint32_t kBarOff = kVOff + kVS * kTileBytes;
 constexpr uint32_t kNumBars = 1 + 2 * kKS + 2 * kVS + 2 * 3 + 2;
-constexpr uint32_t kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+
+// Shared-memory layout for head_dim D (64 or 128): Q of tiles A and B, the
+// K ring, the V ring, then the barriers.
+template <int D> struct Smem {
+    static constexpr uint32_t kTileBytes = kBN * D * 2;  // one K (or V, or Q) tile
+    static constexpr uint32_t kQOff = 0;                 // Q of A, then Q of B
+    static constexpr uint32_t kKOff = kQOff + 2 * kTileBytes;
+    static constexpr uint32_t kVOff = kKOff + kKS * kTileBytes;
+    static constexpr uint32_t kBarOff = kVOff + kVS * kTileBytes;
+    static constexpr uint32_t kBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+};
 constexpr uint64_t kWaitNs = 2000000000ull;     // a role gives up after 2 s on one barrier
 constexpr uint32_t kSleepNs = 20000;            // longest sleep inside one try_wait
 constexpr float kRescaleStep = 8.f;  // raise the running max only when it grows by > 2^8
 constexpr uint32_t kNegInf = 0xff800000u;
 
-// tensor-memory columns of tile x (0 = A, 1 = B)
+// tensor-memory columns of tile x (0 = A, 1 = B): S/P, then O (D columns)
 __device__ inline uint32_t col_s(int x) { return 128u * x; }
-__device__ inline uint32_t col_o(int x) { return 256u + 128u * x; }
+template <int D> __device__ inline uint32_t col_o(int x) { return 256u + uint32_t(D) * x; }
 
 struct TcParams {
     const int32_t* cu_q_lens;
@@ -184,11 +188,14 @@ __device__ inline void apply_mask(uint32_t (&r)[32], uint32_t m) {
     for (int k = 0; k < 32; ++k) r[k] = ((m >> k) & 1u) ? r[k] : kNegInf;
 }
 
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const TcParams a) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int kD = D;
+    constexpr int kHalves = D / 64;  // 64-dim (128-byte) halves of a row
+    constexpr uint32_t kTileBytes = Smem<D>::kTileBytes;
     // The row-tile pairs of one (sequence, kv head) are consecutive CTAs, so
     // they run at the same time and read its K/V tiles through L2 from one
     // DRAM read; within a group the heaviest pairs come first.
@@ -238,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = base + kQOff;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOff);
+    uint8_t* sQ = base + Smem<D>::kQOff;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + Smem<D>::kBarOff);
     uint64_t* q_full = bars;
     uint64_t* k_full = q_full + 1;
     uint64_t* k_empty = k_full + kKS;
@@ -251,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* mma_done = o_done + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars);
     volatile uint32_t* abort_flag = tslot + 1;
-    auto k_tile = [&](int st) { return base + kKOff + st * kTileBytes; };
-    auto v_tile = [&](int st) { return base + kVOff + st * kTileBytes; };
+    auto k_tile = [&](int st) { return base + Smem<D>::kKOff + st * kTileBytes; };
+    auto v_tile = [&](int st) { return base + Smem<D>::kVOff + st * kTileBytes; };
 
     if (tid == 0) {
         mbar_init(q_full, 1);
@@ -298,10 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             // full box bytes count even where the box leaves the tensor (zero fill)
-            const uint32_t qbytes = 2u * 128u * uint32_t(G * tq);
+            const uint32_t qbytes = uint32_t(kHalves) * 128u * uint32_t(G * tq);
             mbar_arrive_expect_tx(q_full, has_b ? 2 * qbytes : qbytes);
             for (int x = 0; x < (has_b ? 2 : 1); ++x)
-                for (int hh = 0; hh < 2; ++hh)
+                for (int hh = 0; hh < kHalves; ++hh)
                     tma_load_3d(sQ + x * kTileBytes + hh * kHalfBytes, &tmQ, q_full, 64 * hh, g * G,
                                 row0 + r_first + x * tq);
         }
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane < PT)
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
+                for (int hh = 0; hh < kHalves; ++hh)
                     tma_load_4d(dst + hh * kHalfBytes + lane * P * 128, map, bar, 64 * hh, xc, yc, pg);
         };
         int kq = 0, vq = 0;  // tiles issued
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O_x += P_x V_j, P_x read from the score columns of tile x
         auto pv = [&](int x, int j) {
             const uint32_t vx = v_lo + (j % kVS) * (kTileBytes >> 4);
-            const uint32_t p_col = tm + col_s(x), o_col = tm + col_o(x);
+            const uint32_t p_col = tm + col_s(x), o_col = tm + col_o<D>(x);
 #pragma unroll
             for (int ks = 0; ks < kBN / 16; ++ks) {
                 // 16 keys: 8-row core groups 1024 B apart, dim halves 16 KB apart.
@@ -435,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = row_ok ? start + r_tile + t + 1 : 0;  // keys [0, lim)
         const float sl2 = a.scale_log2;
         const uint32_t sbase = tm + lane_addr + col_s(x);
-        const uint32_t obase = tm + lane_addr + col_o(x);
+        const uint32_t obase = tm + lane_addr + col_o<D>(x);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         // Table entry of page `lane` of key tile jj (0 for lanes past the
@@ -540,8 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = __all_sync(0xffffffffu, wait_bar(&v_full[sv], (j / kVS) & 1, abort_flag));
                 if (!ok) break;
                 uint8_t* sV = v_tile(sv);
-                for (int i = m; i < (zhi - zlo) * 16; i += kBM) {
-                    const int row = zlo + (i >> 4), c = i & 15;
+                for (int i = m; i < (zhi - zlo) * (kD / 8); i += kBM) {
+                    const int row = zlo + i / (kD / 8), c = i % (kD / 8);
                     *reinterpret_cast<uint4*>(sV + (c >> 3) * kHalfBytes + row * 128 + (c & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -599,24 +606,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <typename T>
+template <typename T, int D>
 cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& p,
                          int n_ctas, cudaStream_t st) {
-    auto kern = prefill_tc<T>;
+    auto kern = prefill_tc<T, D>;
     static bool configured = false;  // benign race: every caller sets the same value
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Smem<D>::kBytes));
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<dim3(n_ctas), kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+    kern<<<dim3(n_ctas), kThreads, Smem<D>::kBytes, st>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool prefill_tc_supported(pa_dtype dt, int D, int P, int G, float scale) {
-    return dt != PA_F32 && D == kD && (P == 16 || P == 32) && G >= 1 && G <= kMaxGroup && scale > 0.f;
+    return dt != PA_F32 && (D == 64 || D == 128) && (P == 16 || P == 32) && G >= 1 && G <= kMaxGroup &&
+           scale > 0.f;
 }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cudaStream_t st) {
@@ -693,8 +702,11 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, int D, int P, cuda
     const int64_t n_ctas = n_pairs * a.num_kv_heads * a.num_seqs;
     if (n_ctas > 0x7fffffff) return cudaErrorInvalidValue;
     p.n_pairs = int32_t(n_pairs);
-    return dt == PA_BF16 ? launch_typed<__nv_bfloat16>(mq, mk, mv, p, int(n_ctas), st)
-                         : launch_typed<__half>(mq, mk, mv, p, int(n_ctas), st);
+    if (D == 64)
+        return dt == PA_BF16 ? launch_typed<__nv_bfloat16, 64>(mq, mk, mv, p, int(n_ctas), st)
+                             : launch_typed<__half, 64>(mq, mk, mv, p, int(n_ctas), st);
+    return dt == PA_BF16 ? launch_typed<__nv_bfloat16, 128>(mq, mk, mv, p, int(n_ctas), st)
+                         : launch_typed<__half, 128>(mq, mk, mv, p, int(n_ctas), st);
 }
 
 }  // namespace pa

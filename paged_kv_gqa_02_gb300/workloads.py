@@ -146,6 +146,18 @@ PACK_BF16 = Workload(name="prefill_16x16_32x8_d128_bf16", kind="prefill", num_se
                      num_kv_heads=8, head_dim=128, page_size=32, q_dtype="bf16", kv_dtype="bf16",
                      context_lens=(16,) * 16, q_lens=(16,) * 16, num_pages=4096, max_blocks_per_seq=1,
                      shuffle=True, scale=1.0 / math.sqrt(128), tol=TOL_16)
-EXTRA = (D256, PACK_F32, PACK_BF16)
+# Crucible's "4x256" prefill shape (4 fresh requests of 256 rows at offset 0,
+# 12 q / 3 kv heads, D64, 16-token pages; crucible paged attention results,
+# the shape table) in f32 on the CUDA cores, and in bf16 on the tensor cores
+# at head_dim 64.
+PACK4_F32 = Workload(name="prefill_4x256_12x3_d64_f32", kind="prefill", num_seqs=4, num_q_heads=12,
+                     num_kv_heads=3, head_dim=64, page_size=16, q_dtype="f32", kv_dtype="f32",
+                     context_lens=(256,) * 4, q_lens=(256,) * 4, num_pages=4096, max_blocks_per_seq=16,
+                     shuffle=True, scale=1.0 / math.sqrt(64), tol=TOL_F32)
+PACK4_BF16 = Workload(name="prefill_4x256_12x3_d64_bf16", kind="prefill", num_seqs=4, num_q_heads=12,
+                      num_kv_heads=3, head_dim=64, page_size=16, q_dtype="bf16", kv_dtype="bf16",
+                      context_lens=(256,) * 4, q_lens=(256,) * 4, num_pages=4096, max_blocks_per_seq=16,
+                      shuffle=True, scale=1.0 / math.sqrt(64), tol=TOL_16)
+EXTRA = (D256, PACK_F32, PACK_BF16, PACK4_F32, PACK4_BF16)
 
 BY_NAME = {w.name: w for w in ALL + EXTRA}

@@ -122,6 +122,12 @@ PREFILL_CASES = [
     (1, 32, 2, 128, 32, (1500,), (100,), "bf16"),
     (2, 24, 2, 128, 32, (400, 260), (260, 260), "f16"),
     (2, 40, 8, 128, 16, (129, 3000), (129, 77), "f16"),
+    # tensor-core path at head_dim 64 (one 64-dim half a row): several group
+    # sizes and both page sizes
+    (2, 12, 3, 64, 16, (100, 300), (37, 300), "bf16"),
+    (3, 32, 4, 64, 32, (1000, 64, 129), (300, 64, 1), "f16"),
+    (2, 16, 16, 64, 32, (257, 2000), (257, 50), "bf16"),
+    (1, 40, 8, 64, 16, (3000,), (129,), "f16"),
 ]
 
 

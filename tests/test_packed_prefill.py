@@ -1,7 +1,8 @@
-"""Packed small-chunk prefill (many short requests in one call) against the
-fp64 oracle at full size: crucible's "16x16" shape (16 fresh requests of 16
-rows, 12 q / 3 kv heads, D64, f32) and the same packing at 32 q / 8 kv
-heads, D128, bf16 on the tensor cores."""
+"""Packed prefill (several requests in one call) against the fp64 oracle at
+full size: crucible's "16x16" shape (16 fresh requests of 16 rows, 12 q /
+3 kv heads, D64, f32), the same packing at 32 q / 8 kv heads, D128, bf16 on
+the tensor cores, and crucible's "4x256" shape (4 fresh requests of 256
+rows, 12 q / 3 kv heads, D64) in f32 and in bf16 on the tensor cores."""
 from __future__ import annotations
 
 import os
@@ -27,7 +28,8 @@ def _lib():
     ops.load()
 
 
-@pytest.mark.parametrize("wl", (workloads.PACK_F32, workloads.PACK_BF16), ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", (workloads.PACK_F32, workloads.PACK_BF16, workloads.PACK4_F32, workloads.PACK4_BF16),
+                         ids=lambda w: w.name)
 def test_packed_prefill_matches_oracle(wl):
     inp = wl.make_inputs()
     p = ops.params_for(wl)
