@@ -2,6 +2,8 @@
 // 5th-generation tensor cores (tcgen05 MMA, accumulators in tensor memory,
 // operands staged by TMA).
 //
+// head_dim 64 or 128 (template parameter D), 16-bit Q/K/V.
+//
 // One CTA per (row-tile pair, kv head, sequence).  The MMA tile's 128 rows are
 // the query heads of one kv head times 128/G consecutive chunk rows
 // (row = token * G + head), so every K/V tile in shared memory serves all
@@ -23,10 +25,11 @@
 //              (O / l to global memory)
 //   warp 8     TMA producer: Q once, then K and V tiles into their rings
 //              (one lane per page issues that page's boxes)
-//   warp 9     tensor-memory owner and MMA issuer (one thread)
+//   warp 9     tensor-memory owner and MMA issuer (the whole warp, converged;
+//              one lane elected to issue each MMA and commit)
 //
 // Tensor memory (512 columns): S/P of tile A [0,128), S/P of tile B
-// [128,256), O of A [256,384), O of B [384,512).  Per key tile j the MMA
+// [128,256), O of A [256,256+D), O of B [256+D,256+2D).  Per key tile j the MMA
 // thread issues P_A(j).V_j, then S_A(j+1) = Q_A K_{j+1}^T once that P.V has
 // finished reading P_A (same columns), then P_B(j).V_j and S_B(j+1): while
 // one warpgroup computes its softmax, the tensor cores work for the other.
