@@ -93,17 +93,6 @@ __device__ inline void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* 
         : "memory");
 }
 
-// As tma_load_4d, with an L2 cache policy (from l2_policy_evict_first).
-__device__ inline void tma_load_4d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                        int c2, int c3, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)),
-        "l"(policy)
-        : "memory");
-}
-
 // A 5-d tile load with an L2 cache policy.
 __device__ inline void tma_load_5d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                         int c2, int c3, int c4, uint64_t policy) {
@@ -132,32 +121,9 @@ __device__ inline void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* 
         : "memory");
 }
 
-__device__ inline void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Pulls a tile of a tensor into L2 ahead of use (no shared memory, no barrier).
-__device__ inline void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
-    asm volatile(
-        "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-        : "memory");
-}
-
 __device__ inline void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
-
-// ---- cp.async (LDGSTS) ------------------------------------------------------------
-__device__ inline void cp_async_4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ inline void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---- ldmatrix / mma.sync ---------------------------------------------------------
 __device__ inline void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -195,23 +161,6 @@ __device__ inline uint32_t movm_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
-}
-
-template <bool kBf16>
-__device__ inline void mma_1688(float* c, uint32_t a0, uint32_t a1, uint32_t b0) {
-    if constexpr (kBf16) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-            "{%4, %5}, {%6}, {%0, %1, %2, %3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(b0));
-    } else {
-        asm volatile(
-            "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-            "{%4, %5}, {%6}, {%0, %1, %2, %3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(b0));
-    }
 }
 
 // ---- inter-CTA counters ------------------------------------------------------------

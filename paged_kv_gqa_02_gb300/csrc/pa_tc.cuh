@@ -30,23 +30,12 @@ __device__ inline void fence_before_sync() { asm volatile("tcgen05.fence::before
 __device__ inline void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // ---- descriptors ------------------------------------------------------------------
-// Shared-memory matrix descriptor (sm_100 family): start address, leading and
-// stride byte offsets (16-byte units), version 1, 128-byte swizzle.
-__device__ inline uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= uint64_t((saddr & 0x3FFFFu) >> 4);
-    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
-    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
-    d |= uint64_t(1) << 46;   // descriptor version for tcgen05
-    d |= uint64_t(2) << 61;   // layout: 128-byte swizzle
-    return d;
-}
-
-// The same descriptor as two 32-bit words: the low word holds the start
-// address and leading byte offset, the high word the stride byte offset,
-// version and layout.  Advancing the start address by `off` bytes inside
-// one shared-memory window adds off >> 4 to the low word (the 14-bit field
-// cannot carry: shared addresses stay below 256 KB).
+// Shared-memory matrix descriptor (sm_100 family) as two 32-bit words: the
+// low word holds the start address and the leading byte offset (16-byte
+// units), the high word the stride byte offset (16-byte units), descriptor
+// version 1 and the 128-byte swizzle layout.  Advancing the start address by
+// `off` bytes inside one shared-memory window adds off >> 4 to the low word
+// (the 14-bit field cannot carry: shared addresses stay below 256 KB).
 __device__ inline uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
     return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
@@ -69,31 +58,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool ab_bf16, boo
 }
 
 // ---- MMA ----------------------------------------------------------------------------
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ inline void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                              bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ inline void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                              bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-        : "memory");
-}
-
-// The same two MMAs issued by one elected lane of a converged warp (the lowest
-// active lane, so always the same lane while the whole warp runs): the warp's
-// operands stay warp-uniform, and the issue needs no divergent branch.
+// D[tmem] (+)= A[smem] * B[smem] (mma_ss_elect) and D[tmem] (+)= A[tmem] *
+// B[smem] (mma_ts_elect), issued by one elected lane of a converged warp (the
+// lowest active lane, so always the same lane while the whole warp runs): the
+// operands stay warp-uniform and the issue needs no divergent branch.
 __device__ inline void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                     bool accumulate) {
     asm volatile(
@@ -114,8 +82,8 @@ __device__ inline void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
         : "memory");
 }
-// commit() from the elected lane of a converged warp (the lane that issued
-// the MMAs through the *_elect forms).
+// Arrives on the mbarrier once every tcgen05 operation issued so far by the
+// elected lane (the one that issues through the *_elect forms) has completed.
 __device__ inline void commit_elect(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -123,14 +91,6 @@ __device__ inline void commit_elect(uint64_t* bar) {
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
             smem_u32(bar))
         : "memory");
-}
-
-// Arrives on the mbarrier once all tcgen05 operations issued so far by this
-// thread have completed.
-__device__ inline void commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
 }
 
 // ---- tensor-memory loads and stores (32 lanes x 32 columns of 32 bits) --------------
@@ -144,18 +104,6 @@ __device__ inline void ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
           "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-}
-
-__device__ inline void st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
 }
 
 __device__ inline void st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -200,11 +148,6 @@ template <int N>
 __device__ inline void reg_fence(uint32_t (&r)[N]) {
 #pragma unroll
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
-}
-
-// Tensor-memory address of (lane, column).
-__device__ inline uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) {
-    return base + (lane << 16) + col;
 }
 
 }  // namespace tc
