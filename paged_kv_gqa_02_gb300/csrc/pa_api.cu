@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include "pa_kernels.h"
+#include "pa_prefill_f32.h"
 
 #define PA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -478,5 +479,7 @@ PA_EXPORT pa_status pa_prefill_chunk(const pa_params* p, const void* q, const in
     a.debug_timeout = p->debug_timeout;
     if (pa::prefill_tc_supported(p->kv_dtype, p->head_dim, p->page_size, r.group, p->scale))
         return cuda_status(pa::launch_prefill_tc(a, p->kv_dtype, p->head_dim, p->page_size, stream));
+    if (p->kv_dtype == PA_F32 && pa::prefill_f32_supported(p->head_dim, p->page_size, r.group))
+        return cuda_status(pa::launch_prefill_f32(a, p->head_dim, p->page_size, stream));
     return cuda_status(pa::launch_prefill_v0(a, p->kv_dtype, p->head_dim, p->page_size, stream));
 }
