@@ -71,7 +71,8 @@ _TOKENS = re.compile(r'"(?:\\.|[^"\\])*"' + r"|'(?:\\.|[^'\\])*'" + r"|//[^\n]*|
 
 # The translation unit each profiled kernel is compiled from.
 KERNEL_FILES = {"decode_v1": "pa_decode_v1.cu", "combine_v1": "pa_decode_v1.cu",
-                "prefill_tc": "pa_prefill_tc.cu", "decode_v0": "pa_tile_v0.cu", "combine_v0": "pa_tile_v0.cu"}
+                "prefill_tc": "pa_prefill_tc.cu", "prefill_f32": "pa_prefill_f32.cu",
+                "decode_v0": "pa_tile_v0.cu", "combine_v0": "pa_tile_v0.cu"}
 _INCLUDE = re.compile(r'^\s*#\s*include\s+"([^"]+)"', re.M)
 
 
