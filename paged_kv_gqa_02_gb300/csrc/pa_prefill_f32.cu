@@ -71,7 +71,11 @@ __global__ void __launch_bounds__(kThr, 1) prefill_f32(const AttnArgs a) {
     int* ok_s = reinterpret_cast<int*>(p_t + kKB * kPld);  // [2 buffers][kKB]: key in a pool page
 
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int b = blockIdx.z, g = blockIdx.y, tile = blockIdx.x;
+    // grid (kv head x sequence, tile), tiles launched latest rows (most keys)
+    // first across all (sequence, kv head) pairs, so a last partial wave
+    // holds the lightest tiles
+    const int g = int(blockIdx.x) % a.num_kv_heads, b = int(blockIdx.x) / a.num_kv_heads;
+    const int tile = int(gridDim.y - 1 - blockIdx.y);
     const int G = a.group, Hq = a.num_q_heads;
     const int tq = kM / G;  // chunk rows of a tile
 
@@ -285,7 +289,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t st) {
     }
     const int tq = kM / a.group;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned((a.max_q_len + tq - 1) / tq), unsigned(a.num_kv_heads), unsigned(a.num_seqs));
+    cfg.gridDim = dim3(unsigned(a.num_kv_heads) * unsigned(a.num_seqs), unsigned((a.max_q_len + tq - 1) / tq));
     cfg.blockDim = dim3(kThr);
     cfg.dynamicSmemBytes = sm;
     cfg.stream = st;
@@ -306,6 +310,8 @@ bool prefill_f32_supported(int D, int P, int G) {
 cudaError_t launch_prefill_f32(const AttnArgs& in, int D, int P, cudaStream_t st) {
     if (!prefill_f32_supported(D, P, in.group) || in.out == nullptr || in.cu_q_lens == nullptr)
         return cudaErrorInvalidValue;
+    const int64_t tiles = (int64_t(in.max_q_len) + kM / in.group - 1) / (kM / in.group);
+    if (int64_t(in.num_kv_heads) * in.num_seqs > 0x7fffffff || tiles > 65535) return cudaErrorInvalidValue;
     AttnArgs a = in;
     a.q_elems = a.out_elems = int64_t(a.total_q) * a.num_q_heads * D;
     if (D == 64) return P == 16 ? launch<64, 16>(a, st) : launch<64, 32>(a, st);
