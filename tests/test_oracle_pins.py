@@ -406,6 +406,17 @@ def test_workload_visible_keys_match_pages():
         assert w.visible_keys() == want
 
 
+def test_named_packed_workloads_are_the_pages_shapes():
+    """The bench's packed-prefill workloads are the pages' 16x16 and 4x256
+    shapes: their causal bound is the printed sum of causal positions."""
+    want = {name: s for name, _, _, s in read_causal_golden()}
+    for wl in (workloads.PACK_F32, workloads.PACK_BF16):
+        assert wl.visible_keys() == want["16x16"]
+    for wl in (workloads.PACK4_F32, workloads.PACK4_BF16):
+        assert wl.visible_keys() == want["4x256"]
+        assert wl.flops() == 4 * want["4x256"] * wl.num_q_heads * wl.head_dim
+
+
 def test_generator_lengths_and_stream():
     """The ragged batch lengths: forced 1/31/32/33 then seeded draws."""
     L = inputs.ragged_lengths(inputs.DEFAULT_SEED, 12)
