@@ -624,7 +624,7 @@ __global__ void __maxnreg__(224)
             const int ntok = min(P, rem);
             // ---- K tile: S^T = K Q^T, masked, online softmax
             bool ok = !timed_out;
-            // every lane waits (each needs the barrier's ordering); one verdict per warp
+            // every lane waits (each needs the barrier's ordering); one outcome per warp
             if (ok && !__all_sync(0xffffffffu, mbar_wait_ns(&my_full[x % NH], (x / NH) & 1, kWaitNs))) {
                 timed_out = true;
                 x_stop = x;
