@@ -7,7 +7,8 @@
 // online-softmax experiment), base-2 exponentials.
 //
 // It serves four roles: the decode split partial (R = 1 row per sequence),
-// the chunked-prefill kernel (R rows per tile, causal per row), the
+// the chunked-prefill kernel for the shapes the tensor-core and fp32
+// prefill kernels do not take (R rows per tile, causal per row), the
 // multi-row decode split partial (row tiles x key splits), and the fp32-KV
 // decode path.  The split combine is at the end of this file.
 #include "pa_common.cuh"
